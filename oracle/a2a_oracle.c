@@ -1,0 +1,285 @@
+/*
+ * a2a_oracle.c -- plain CPU oracle for the EP-MoE all-to-all permutations.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the package's
+ * smoke check and the benchmark's CPU-baseline leg may build, load or call
+ * this file.  It shares no code, header, table or helper with the CUDA path:
+ * every function here is the plain definition written out as nested loops,
+ * copying `es` bytes per element with memcpy (no arithmetic on the values, so
+ * any dtype -- including NaN payloads and -0 -- passes through bit for bit).
+ *
+ * Layouts (all contiguous, rank-major, row-major inside a rank):
+ *   combine      in  [W][S*W][H][D]   out [W][S][H*W][D]
+ *   dispatch     in  [W][S][H][D]     out [W][S/W][H*W][D]
+ *   combine_back in  [W][Sp][H*W][D]  out [W][Sp*W][H][D]     (Sp = S/W)
+ *
+ * Return value: 0 on success, -1 on an invalid shape.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Reverse All2All (combine).
+ * Source: "Reverse All2All (EP MoE Distributed Kernel)", section "Reverse
+ * All2All Operator Semantics": per rank the input (S*world_size, H, D) becomes
+ * the output (S, H*world_size, D).  Which input row lands in which output
+ * column follows the same page's "MTE Implementation": the producer of rank
+ * r reads row target*S + s, expert column h, and writes the target's column
+ * r*H + h; the consumer of rank d keeps row s and column r*H + h.  Hence
+ *     out_d[s, r*H + h, x] = in_r[d*S + s, h, x].                            */
+int oracle_combine(const void *in, void *out, int64_t W, int64_t S, int64_t H,
+                   int64_t D, int64_t es)
+{
+    if (W < 1 || S < 0 || H < 0 || D < 0 || es < 1) return -1;
+    const unsigned char *src = (const unsigned char *)in;
+    unsigned char *dst = (unsigned char *)out;
+    for (int64_t d = 0; d < W; d++)
+        for (int64_t s = 0; s < S; s++)
+            for (int64_t r = 0; r < W; r++)
+                for (int64_t h = 0; h < H; h++)
+                    for (int64_t x = 0; x < D; x++) {
+                        /* in_r has S*W rows of H*D elements */
+                        int64_t i_in = ((r * (S * W) + (d * S + s)) * H + h) * D + x;
+                        /* out_d has S rows of (H*W)*D elements */
+                        int64_t i_out = ((d * S + s) * (H * W) + (r * H + h)) * D + x;
+                        memcpy(dst + i_out * es, src + i_in * es, (size_t)es);
+                    }
+    return 0;
+}
+
+/* Forward All2All (dispatch).
+ * Source: same page, "Reverse All2All Operator Semantics" and "EP MoE
+ * Scenario": per rank (S, H, D) becomes (S/world_size, H*world_size, D).  The
+ * page gives shapes only; the row/column placement is the combine's with the
+ * block length S' = S/W:
+ *     out_d[s', r*H + h, x] = in_r[d*S' + s', h, x].
+ * S must be a multiple of W.                                                 */
+int oracle_dispatch(const void *in, void *out, int64_t W, int64_t S, int64_t H,
+                    int64_t D, int64_t es)
+{
+    if (W < 1 || S < 0 || H < 0 || D < 0 || es < 1 || S % W != 0) return -1;
+    const int64_t Sp = S / W;
+    const unsigned char *src = (const unsigned char *)in;
+    unsigned char *dst = (unsigned char *)out;
+    for (int64_t d = 0; d < W; d++)
+        for (int64_t sp = 0; sp < Sp; sp++)
+            for (int64_t r = 0; r < W; r++)
+                for (int64_t h = 0; h < H; h++)
+                    for (int64_t x = 0; x < D; x++) {
+                        /* in_r has S rows of H*D elements */
+                        int64_t i_in = ((r * S + (d * Sp + sp)) * H + h) * D + x;
+                        /* out_d has Sp rows of (H*W)*D elements */
+                        int64_t i_out = ((d * Sp + sp) * (H * W) + (r * H + h)) * D + x;
+                        memcpy(dst + i_out * es, src + i_in * es, (size_t)es);
+                    }
+    return 0;
+}
+
+/* Inverse of dispatch ("results must be sent back ... to the token's original
+ * rank", same page, introduction).  Per rank (Sp, H*W, D) becomes (Sp*W, H, D):
+ *     out_r[d*Sp + s', h, x] = in_d[s', r*H + h, x].                         */
+int oracle_combine_back(const void *in, void *out, int64_t W, int64_t Sp,
+                        int64_t H, int64_t D, int64_t es)
+{
+    if (W < 1 || Sp < 0 || H < 0 || D < 0 || es < 1) return -1;
+    const unsigned char *src = (const unsigned char *)in;
+    unsigned char *dst = (unsigned char *)out;
+    for (int64_t r = 0; r < W; r++)
+        for (int64_t d = 0; d < W; d++)
+            for (int64_t sp = 0; sp < Sp; sp++)
+                for (int64_t h = 0; h < H; h++)
+                    for (int64_t x = 0; x < D; x++) {
+                        /* in_d has Sp rows of (H*W)*D elements */
+                        int64_t i_in = ((d * Sp + sp) * (H * W) + (r * H + h)) * D + x;
+                        /* out_r has Sp*W rows of H*D elements */
+                        int64_t i_out = ((r * (Sp * W) + (d * Sp + sp)) * H + h) * D + x;
+                        memcpy(dst + i_out * es, src + i_in * es, (size_t)es);
+                    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sequential replay of the tile-level producer/consumer algorithm of the    */
+/* page's "MTE Implementation" (sections "Producer-Consumer Pipeline",       */
+/* "Signal Memory Layout", "Symmetric Memory Layout").  It exists to pin the  */
+/* definition above against the page's own index arithmetic: the staging     */
+/* ("peer memory") layout [buffer][block_s rows][H*W][D] per rank, the        */
+/* per-task int64 signal slots spaced 8 elements apart, the wait-for-0 /      */
+/* notify-1 / wait-for-1 / reset-to-0 handshake, and the boundary masks.      */
+/*                                                                            */
+/* Every "core" of the page runs one after another: within one S block all    */
+/* producer tasks of every rank, then all consumer tasks of every rank.  That */
+/* is one legal interleaving of the concurrent pipeline.  A wait whose        */
+/* condition does not hold in this order is a protocol error (returns -2).    */
+/*                                                                            */
+/* staging: W * buffer_num * block_s * (H*W) * D * es bytes (rank-major)      */
+/* signals: W * buffer_num * nbd * H * W * 8 int64 (rank-major), zeroed by    */
+/*          the caller first, as the page's host side does before launch.     */
+/* ------------------------------------------------------------------------ */
+int oracle_pc_replay(const void *in, void *out, int64_t W, int64_t S, int64_t H,
+                     int64_t D, int64_t es, int64_t block_s, int64_t block_d,
+                     int64_t buffer_num, void *staging, int64_t *signals)
+{
+    if (W < 1 || S < 0 || H < 0 || D < 0 || es < 1 || block_s < 1 || block_d < 1 ||
+        buffer_num < 1)
+        return -1;
+    const unsigned char *a = (const unsigned char *)in;
+    unsigned char *c = (unsigned char *)out;
+    unsigned char *peer = (unsigned char *)staging;
+    const int64_t nbs = (S + block_s - 1) / block_s;
+    const int64_t nbd = (D + block_d - 1) / block_d;
+    const int64_t tasks = nbd * H * W;                 /* per buffer, per rank */
+    const int64_t chunk = H * W * D;                   /* one staging row      */
+    const int64_t peer_rank_elems = buffer_num * block_s * chunk;
+    const int64_t sig_rank_elems = buffer_num * tasks * 8;
+    const int64_t a_rank_rows = S * W;                 /* input rows per rank  */
+
+    for (int64_t bs = 0; bs < nbs; bs++) {
+        const int64_t buf = bs % buffer_num;
+
+        /* producers: every source rank, every task (rank_loop, h, d block) */
+        for (int64_t rank = 0; rank < W; rank++) {
+            for (int64_t task = 0; task < tasks; task++) {
+                const int64_t rank_loop = task % W;
+                const int64_t hd = task / W;           /* = block_d*H + h */
+                const int64_t h = hd % H;
+                const int64_t bd = hd / H;
+                const int64_t target = (rank + rank_loop) % W;
+                int64_t *slot = signals + target * sig_rank_elems +
+                                (buf * tasks + rank * nbd * H + hd) * 8;
+                if (*slot != 0) return -2;             /* wait(slot == 0) */
+                for (int64_t i = 0; i < block_s; i++) {
+                    const int64_t s = bs * block_s + i;
+                    if (s >= S) continue;              /* row mask */
+                    for (int64_t j = 0; j < block_d; j++) {
+                        const int64_t x = bd * block_d + j;
+                        if (x >= D) continue;          /* column mask */
+                        const int64_t i_a = ((rank * a_rank_rows + target * S + s) * H + h) * D + x;
+                        const int64_t i_p = target * peer_rank_elems +
+                                            (buf * block_s + i) * chunk +
+                                            (rank * H + h) * D + x;
+                        memcpy(peer + i_p * es, a + i_a * es, (size_t)es);
+                    }
+                }
+            }
+            /* after its fence, the producer notifies every task's slot */
+            for (int64_t task = 0; task < tasks; task++) {
+                const int64_t hd = task / W;
+                const int64_t target = (rank + task % W) % W;
+                signals[target * sig_rank_elems + (buf * tasks + rank * nbd * H + hd) * 8] = 1;
+            }
+        }
+
+        /* consumers: every destination rank, every task (r, h, d block) */
+        for (int64_t rank = 0; rank < W; rank++) {
+            for (int64_t task = 0; task < tasks; task++) {
+                const int64_t r = task % W;
+                const int64_t hd = task / W;
+                const int64_t h = hd % H;
+                const int64_t bd = hd / H;
+                const int64_t *slot = signals + rank * sig_rank_elems +
+                                      (buf * tasks + r * nbd * H + hd) * 8;
+                if (*slot != 1) return -2;             /* wait(slot == 1) */
+                for (int64_t i = 0; i < block_s; i++) {
+                    const int64_t s = bs * block_s + i;
+                    if (s >= S) continue;
+                    for (int64_t j = 0; j < block_d; j++) {
+                        const int64_t x = bd * block_d + j;
+                        if (x >= D) continue;
+                        const int64_t i_p = rank * peer_rank_elems +
+                                            (buf * block_s + i) * chunk +
+                                            (r * H + h) * D + x;
+                        const int64_t i_c = ((rank * S + s) * (H * W) + (r * H + h)) * D + x;
+                        memcpy(c + i_c * es, peer + i_p * es, (size_t)es);
+                    }
+                }
+            }
+            /* after its fence, the consumer returns every slot to 0 */
+            for (int64_t task = 0; task < tasks; task++) {
+                const int64_t r = task % W;
+                const int64_t hd = task / W;
+                signals[rank * sig_rank_elems + (buf * tasks + r * nbd * H + hd) * 8] = 0;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* One-sided primitives on a symmetric heap held in host memory.              */
+/* Source: "Distributed Architecture Design" section 5.3 (remote address =    */
+/* target PE's heap base + the pointer's offset from the local heap base),    */
+/* and the HyperParallel "Symmetric Memory" RFC, section 4 (Python API) and   */
+/* section 6 (primitive semantics): put copies size bytes to the target PE,   */
+/* get copies from the source PE, signal_op is SET (0) or ADD (1), wait       */
+/* compares with EQ (0), GT (1) or LT (2).                                    */
+/* The heap here is npes slabs of slab_stride bytes, slab k = PE k.           */
+/* ------------------------------------------------------------------------ */
+
+/* Address of `offset` (bytes from the start of a slab) on PE `pe`. */
+static unsigned char *oracle_heap_at(unsigned char *heap, int64_t slab_stride,
+                                     int64_t pe, int64_t offset)
+{
+    return heap + pe * slab_stride + offset;
+}
+
+/* put: target slab `pe`, byte offset target_off, receives `bytes` from src. */
+int oracle_put(void *heap, int64_t slab_stride, int64_t npes, int64_t target_off,
+               const void *src, int64_t bytes, int64_t pe)
+{
+    if (pe < 0 || pe >= npes || target_off < 0 || bytes < 0 ||
+        target_off + bytes > slab_stride)
+        return -1;
+    memcpy(oracle_heap_at((unsigned char *)heap, slab_stride, pe, target_off), src,
+           (size_t)bytes);
+    return 0;
+}
+
+/* get: dst receives `bytes` from slab `pe` at byte offset src_off. */
+int oracle_get(const void *heap, int64_t slab_stride, int64_t npes, void *dst,
+               int64_t src_off, int64_t bytes, int64_t pe)
+{
+    if (pe < 0 || pe >= npes || src_off < 0 || bytes < 0 || src_off + bytes > slab_stride)
+        return -1;
+    memcpy(dst, oracle_heap_at((unsigned char *)heap, slab_stride, pe, src_off),
+           (size_t)bytes);
+    return 0;
+}
+
+/* signal_op on the int64 signal at byte offset sig_off of slab `pe`. */
+int oracle_signal_op(void *heap, int64_t slab_stride, int64_t npes, int64_t sig_off,
+                     int64_t value, int64_t op, int64_t pe)
+{
+    if (pe < 0 || pe >= npes || sig_off < 0 || sig_off + 8 > slab_stride) return -1;
+    int64_t cur;
+    unsigned char *p = oracle_heap_at((unsigned char *)heap, slab_stride, pe, sig_off);
+    memcpy(&cur, p, 8);
+    if (op == 0)
+        cur = value;                                  /* SET */
+    else if (op == 1)
+        cur = (int64_t)((uint64_t)cur + (uint64_t)value); /* ADD, wrapping */
+    else
+        return -1;
+    memcpy(p, &cur, 8);
+    return 0;
+}
+
+/* wait predicate: 1 if `current` satisfies (cmp, value), 0 if not, -1 bad cmp */
+int oracle_wait_satisfied(int64_t current, int64_t value, int64_t cmp)
+{
+    if (cmp == 0) return current == value;            /* EQ */
+    if (cmp == 1) return current > value;             /* GT */
+    if (cmp == 2) return current < value;             /* LT */
+    return -1;
+}
+
+/* put_with_signal: the data lands before the signal changes (the RFC's     */
+/* "fence before signal" rule); sequentially that is put, then signal_op.   */
+int oracle_put_with_signal(void *heap, int64_t slab_stride, int64_t npes,
+                           int64_t target_off, const void *src, int64_t bytes,
+                           int64_t sig_off, int64_t value, int64_t op, int64_t pe)
+{
+    int rc = oracle_put(heap, slab_stride, npes, target_off, src, bytes, pe);
+    if (rc) return rc;
+    return oracle_signal_op(heap, slab_stride, npes, sig_off, value, op, pe);
+}
