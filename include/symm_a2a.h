@@ -1,0 +1,224 @@
+/*
+ * symm_a2a.h -- C ABI of the GB300 symmetric-heap all-to-all library
+ * (libsymm_a2a.so, sm_103a).
+ *
+ * W processing elements (PEs, "ranks") are emulated on one GPU as W equal
+ * slabs of one device allocation that the caller owns.  Every call takes
+ * plain pointers and sizes; device pointers are marked "device", the CUDA
+ * stream is passed as `void *stream` (a cudaStream_t; NULL = legacy default
+ * stream).  Calls that launch work are asynchronous on that stream: a zero
+ * return means "validated and enqueued".  A wait that gives up on the device
+ * is reported later by symm_check_error().
+ *
+ * Return codes: SYMM_OK, or a negative SYMM_E* code; symm_last_error() then
+ * holds a one-line message (per calling thread).  No call allocates device
+ * memory; none frees memory it did not allocate; none ever traps the GPU.
+ *
+ * Sources (page, section) of the operations:
+ *  [RA2A]  "Reverse All2All (EP MoE Distributed Kernel)": sections "Reverse
+ *          All2All Operator Semantics", "EP MoE Scenario", "MTE
+ *          Implementation" (Producer-Consumer Pipeline, Signal Memory Layout,
+ *          Symmetric Memory Layout, Performance Considerations).
+ *  [RFC]   HyperParallel RFC "Symmetric Memory (one-sided communication)":
+ *          section 2 (symmetric memory), 4 (Python API), 5 (push/pull
+ *          modes), 6 (primitive semantics), 8 (kernel notes).
+ *  [ARCH]  "Distributed Architecture Design": section 5 (symmetric heap
+ *          runtime, 5.3 symm_at address resolution), section 6 (signal,
+ *          wait, fence mechanisms).
+ */
+#ifndef SYMM_A2A_H
+#define SYMM_A2A_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- codes -- */
+#define SYMM_OK 0
+#define SYMM_EINVAL (-1)    /* bad argument: shape, PE, pointer, range, alignment */
+#define SYMM_ENOMEM (-2)    /* the heap's slab has no room for the request */
+#define SYMM_ETIMEDOUT (-3) /* a device-side wait ran past its budget */
+#define SYMM_ECUDA (-4)     /* a CUDA runtime call failed (message in symm_last_error) */
+
+/* signal operations and comparisons, numbered as the [RFC] Python API numbers
+ * them (section 4: signal_op 0=SET, 1=ADD; compare_op 0=EQ, 1=GT, 2=LT) */
+#define SYMM_SIGNAL_SET 0
+#define SYMM_SIGNAL_ADD 1
+#define SYMM_CMP_EQ 0
+#define SYMM_CMP_GT 1
+#define SYMM_CMP_LT 2
+
+/* all2all_combine variants */
+#define SYMM_A2A_DIRECT 0 /* one pass over every (source, destination, row) run */
+#define SYMM_A2A_PC 1     /* persistent producer/consumer through staging slots */
+/* OR-ed into the variant: skip the signal reset that precedes a PC launch
+ * (the caller has zeroed the signal slots itself) */
+#define SYMM_A2A_FLAG_NO_RESET 0x100
+
+/* bytes at the start of every slab that the heap keeps for itself */
+#define SYMM_HEAP_HEADER_BYTES 4096
+/* distance between two producer/consumer signal slots (one 64-byte line) */
+#define SYMM_SIGNAL_STRIDE_BYTES 64
+
+typedef struct symm_heap symm_heap_t;
+
+/* ------------------------------------------------------- symmetric heap -- */
+
+/* [ARCH] 5, [RFC] 2: a symmetric heap is memory of the same size and layout
+ * on every PE, so an offset means the same object on every PE.
+ * base        device; caller-owned; >= npes * slab_stride bytes; 256-byte
+ *             aligned.  The heap never frees it.  The first
+ *             SYMM_HEAP_HEADER_BYTES of every slab are reserved.
+ * slab_stride bytes per PE; a multiple of 256 (2 MiB recommended) and
+ *             > SYMM_HEAP_HEADER_BYTES.  PE k's slab starts at base + k*slab_stride.
+ * npes        number of PEs (W), >= 1.
+ * heap        out: host handle.  Touches no device memory (the header is
+ *             zeroed on the stream of the first call that launches work).
+ * Errors: SYMM_EINVAL. */
+int symm_heap_init(void *base, size_t slab_stride, int npes, symm_heap_t **heap);
+
+/* Releases the host handle only. */
+int symm_heap_destroy(symm_heap_t *heap);
+
+/* [ARCH] 5.2 (symmetric allocation: same size on every PE).  Bump-allocates
+ * `bytes` at one offset, reserved in every slab; returns PE 0's address.
+ * align: power of two (0 = 256); the result is always 256-byte aligned and
+ * every allocation is padded to a multiple of 256 bytes.
+ * Errors: SYMM_EINVAL (bad align), SYMM_ENOMEM (slab full). */
+int symm_malloc(symm_heap_t *heap, size_t bytes, size_t align, void **ptr);
+
+/* Frees every symm_malloc allocation at once (offsets restart after the header). */
+int symm_heap_reset(symm_heap_t *heap);
+
+/* [ARCH] 5.3: the address of `ptr`'s object on PE `pe`:
+ *   base + pe*slab_stride + ((ptr - base) mod slab_stride).
+ * ptr may point into any slab.  Returns NULL when pe is out of range or ptr
+ * is outside the heap.  Host-only arithmetic. */
+void *symm_at(symm_heap_t *heap, const void *ptr, int pe);
+
+/* Default spin budget of producer/consumer waits, in ns (initially 2 s). */
+int symm_set_spin_budget(symm_heap_t *heap, uint64_t budget_ns);
+
+/* Synchronises `stream`, then returns the first device-side error recorded in
+ * the heap header since the last check (SYMM_OK or SYMM_ETIMEDOUT) and clears
+ * it.  Until it is cleared, every later device wait on this heap gives up at
+ * once (the abort flag stays raised), so check after any launch that may
+ * have timed out.  *info (optional) receives the byte offset from base of the signal that
+ * timed out.  Errors: SYMM_ECUDA. */
+int symm_check_error(symm_heap_t *heap, void *stream, int64_t *info);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *symm_last_error(void);
+
+/* ------------------------------------------------- one-sided primitives -- */
+
+/* [RFC] 4, 6 (shmem_put; push): copy `bytes` from device src + src_off to
+ * PE target_pe's copy of the symmetric object `target`, at byte target_off.
+ * The destination range must lie in one slab past the header; src is any
+ * device memory inside a 16-byte-aligned allocation (cudaMalloc, torch).
+ * Any alignment of either side.  Errors: SYMM_EINVAL. */
+int shmem_put(symm_heap_t *heap, void *target, size_t target_off, const void *src,
+              size_t src_off, size_t bytes, int target_pe, void *stream);
+
+/* [RFC] 4, 6 (shmem_get; pull): copy `bytes` from PE src_pe's copy of the
+ * symmetric object `src`, at byte src_off, to device dst + dst_off. */
+int shmem_get(symm_heap_t *heap, void *dst, size_t dst_off, const void *src, size_t src_off,
+              size_t bytes, int src_pe, void *stream);
+
+/* [RFC] 4, 6; [ARCH] 6.2: apply SET or ADD of `value` to the int64 at
+ * element `signal_off` of PE target_pe's copy of the symmetric array
+ * `signal` (8-byte aligned), with release semantics at GPU scope: writes
+ * ordered before this call on the stream are visible to whoever observes
+ * the new value.  op: SYMM_SIGNAL_SET or SYMM_SIGNAL_ADD (wrapping). */
+int shmem_signal_op(symm_heap_t *heap, int64_t *signal, size_t signal_off, int64_t value, int op,
+                    int target_pe, void *stream);
+
+/* [RFC] 4, 6; [ARCH] 6.3: block the stream until the int64 at element
+ * signal_off of PE pe's copy of `signal` compares (cmp: EQ/GT/LT) true
+ * against cmp_value, with acquire semantics; work later on the stream sees
+ * what the signaller wrote before its signal.  The wait does not consume the
+ * signal (several waiters may wait on one slot).  It gives up after
+ * budget_ns (0 = the heap's spin budget) and then records SYMM_ETIMEDOUT for
+ * symm_check_error(); it never hangs the GPU.  Another kernel that must run
+ * concurrently to satisfy it is not guaranteed to: signal first in stream
+ * order, or expect the timeout. */
+int shmem_wait_for_signal(symm_heap_t *heap, const int64_t *signal, size_t signal_off,
+                          int64_t cmp_value, int cmp, int pe, uint64_t budget_ns, void *stream);
+
+/* [RFC] 4, 6, 8 (put_mem_signal): shmem_put, then -- after every byte of it
+ * is visible at GPU scope -- shmem_signal_op on PE target_pe, in one launch.
+ * Calls of it that overlap on the device share one arrival counter in the
+ * heap header and race; issue them in stream order. */
+int shmem_put_with_signal(symm_heap_t *heap, void *target, size_t target_off, const void *src,
+                          size_t src_off, size_t bytes, int64_t *signal, size_t signal_off,
+                          int64_t value, int op, int target_pe, void *stream);
+
+/* ------------------------------------------------------------ all-to-all -- */
+
+/* Sizes of the producer/consumer workspace, per PE ([RA2A] "Signal Memory
+ * Layout", "Symmetric Memory Layout"):
+ *   staging : buffer_num * tile_s * (H*W) * D * elem_bytes bytes
+ *             (layout [buffer][tile_s rows][H*W][D])
+ *   signals : buffer_num * nbd * H * W slots of SYMM_SIGNAL_STRIDE_BYTES
+ *             (int64 each; slot (buf, r, bd, h) at
+ *              ((buf*W + r)*nbd + bd)*H + h), nbd = ceil(D / block_d).
+ * block_d = 0 means D.  Errors: SYMM_EINVAL. */
+int all2all_pc_workspace(int W, int S, int H, int D, int elem_bytes, int tile_s, int block_d,
+                         int buffer_num, size_t *staging_bytes, size_t *signal_bytes);
+
+/* [RA2A] "Reverse All2All Operator Semantics" / "MTE Implementation":
+ * Reverse All2All (combine).  Per PE the input (S*W, H, D) becomes the
+ * output (S, H*W, D):
+ *     out_d[s, r*H + h, x] = in_r[d*S + s, h, x]
+ * for every destination PE d, source PE r, row s < S, h < H, x < D.
+ * in, out     symmetric (heap) pointers; PE k's tensors are symm_at(in|out, k),
+ *             contiguous row-major, elem_bytes per element, any alignment.
+ *             The input and output ranges must not overlap.
+ * variant     SYMM_A2A_DIRECT, or SYMM_A2A_PC [| SYMM_A2A_FLAG_NO_RESET]:
+ *             producers copy tile_s x block_d tiles of every source PE into
+ *             the destination PE's staging slot and release its signal; the
+ *             destination's consumers acquire it, copy the tile into the
+ *             output and return the slot (signal 0).  The launch zeroes the
+ *             W signal arrays first (unless NO_RESET).  Its grid never
+ *             exceeds the CTAs that fit on the GPU at once.
+ * tile_s, block_d, buffer_num, staging, signals: PC only (see
+ *             all2all_pc_workspace; staging and signals are symmetric
+ *             pointers of at least those sizes); ignored by DIRECT.
+ * elem_bytes  any size >= 1; values move as raw bits.
+ * S, H or D = 0 is a no-op.  Errors: SYMM_EINVAL, SYMM_ECUDA; a PC wait that
+ * gives up shows in symm_check_error(). */
+int all2all_combine(symm_heap_t *heap, const void *in, void *out, int W, int S, int H, int D,
+                    int elem_bytes, int variant, int tile_s, int block_d, int buffer_num,
+                    void *staging, int64_t *signals, void *stream);
+
+/* [RA2A] "Reverse All2All Operator Semantics" / "EP MoE Scenario": Forward
+ * All2All (dispatch).  Per PE (S, H, D) becomes (S/W, H*W, D):
+ *     out_d[s', r*H + h, x] = in_r[d*S' + s', h, x],   S' = S/W.
+ * S % W != 0 is SYMM_EINVAL.  Same pointer rules as all2all_combine. */
+int all2all_dispatch(symm_heap_t *heap, const void *in, void *out, int W, int S, int H, int D,
+                     int elem_bytes, void *stream);
+
+/* Inverse of all2all_dispatch (results returned to the tokens' ranks,
+ * [RA2A] introduction).  Per PE (Sp, H*W, D) becomes (Sp*W, H, D):
+ *     out_r[d*Sp + s', h, x] = in_d[s', r*H + h, x]. */
+int all2all_combine_back(symm_heap_t *heap, const void *in, void *out, int W, int Sp, int H,
+                         int D, int elem_bytes, void *stream);
+
+/* all2all_combine on host buffers: copies host_in ([W][S*W][H][D],
+ * contiguous) into the W input slabs, runs the combine, and copies the W
+ * output slabs to host_out ([W][S][H*W][D]), all on `stream` with one
+ * cudaMemcpyAsync per slab and direction.  Page-locked host buffers make the
+ * copies asynchronous.  Returns once enqueued. */
+int all2all_combine_host(symm_heap_t *heap, const void *host_in, void *host_out, const void *in,
+                         void *out, int W, int S, int H, int D, int elem_bytes, int variant,
+                         int tile_s, int block_d, int buffer_num, void *staging, int64_t *signals,
+                         void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SYMM_A2A_H */

@@ -1,0 +1,266 @@
+// symm_device.cuh -- device-side building blocks of the symmetric-heap library
+// (sm_103a): scoped release/acquire on int64 signals, a bounded spin, and
+// warp-cooperative byte copies that keep 16-byte vector loads and stores on
+// any source/destination alignment.
+//
+// Memory-model notes.  All W emulated PEs live on one GPU, so ".gpu" scope is
+// the scope of every signal.  A signal is released by one thread after a
+// named barrier of its group (the group's stores are ordered before the
+// release through the barrier, then the release fence), and acquired by one
+// thread before a named barrier (the group's later loads are ordered after
+// the acquire).  Data that may change while a kernel runs (staging slots,
+// one-sided put/get sources) is read with ld.global.cg (L2 only), never
+// through the non-coherent path; inputs that are read-only for the whole
+// launch use ld.global.nc with L1::no_allocate.
+#pragma once
+
+#include <stdint.h>
+
+namespace symm {
+
+// ---------------------------------------------------------------- scalars --
+__device__ __forceinline__ int64_t ld_acquire(const int64_t* p) {
+  int64_t v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int64_t ld_relaxed(const int64_t* p) {
+  int64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int64_t* p, int64_t v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_release(int64_t* p, int64_t v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+__device__ __forceinline__ void fence_acq_rel() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Named barrier over `nthreads` threads (a multiple of 32) of this CTA.
+__device__ __forceinline__ void group_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------ control block ------
+// Lives in the first bytes of slab 0 of every heap (the heap header).
+struct Control {
+  int32_t error;       // 0 or a negative SYMM_E* code (first error wins)
+  uint32_t abort;      // set once any waiter gives up; every spin then returns
+  int64_t error_info;  // byte offset (from the heap base) of the signal that timed out
+  uint32_t done;       // CTA arrival counter of shmem_put_with_signal
+  uint32_t pad0;
+  int64_t reserved[5];
+};
+
+enum { kCmpEq = 0, kCmpGt = 1, kCmpLt = 2 };
+enum { kSpinOk = 0, kSpinTimeout = 1, kSpinAborted = 2 };
+enum { kErrTimedOut = -3 };
+
+__device__ __forceinline__ bool cmp_holds(int64_t cur, int cmp, int64_t v) {
+  return cmp == kCmpEq ? cur == v : (cmp == kCmpGt ? cur > v : cur < v);
+}
+
+__device__ __forceinline__ void record_timeout(Control* ctl, const void* heap_base,
+                                               const int64_t* sig) {
+  if (atomicCAS(reinterpret_cast<int*>(&ctl->error), 0, kErrTimedOut) == 0)
+    ctl->error_info = (int64_t)((const char*)sig - (const char*)heap_base);
+  st_relaxed_u32(&ctl->abort, 1u);
+}
+
+// Spin (one thread) until `*sig cmp v` holds, with acquire semantics.  Gives
+// up after `budget_ns` of %globaltimer time, or after an iteration cap that
+// bounds the wait even if the timer stood still, or as soon as another waiter
+// has raised the abort flag.  Never traps.
+__device__ __forceinline__ int spin_wait(const int64_t* sig, int cmp, int64_t v, uint64_t budget_ns,
+                                         Control* ctl, const void* heap_base) {
+  const uint64_t t0 = globaltimer_ns();
+  // each round sleeps >= 64 ns, so this cap is >= ~budget/2 of wall time
+  const uint64_t max_iters = budget_ns / 128 + 4096;
+  uint32_t backoff = 32;
+  for (uint64_t it = 0;; ++it) {
+    if (cmp_holds(ld_acquire(sig), cmp, v)) return kSpinOk;
+    if (ld_relaxed_u32(&ctl->abort)) return kSpinAborted;
+    if (globaltimer_ns() - t0 > budget_ns || it > max_iters) {
+      record_timeout(ctl, heap_base, sig);
+      return kSpinTimeout;
+    }
+    __nanosleep(backoff);
+    if (backoff < 256) backoff <<= 1;
+  }
+}
+
+// -------------------------------------------------------------- vectors ---
+// Read-only-for-the-launch input: non-coherent path, no L1 allocation.
+__device__ __forceinline__ uint4 ld16_ro(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+// Data another thread may have written during this launch: L2 only.
+__device__ __forceinline__ uint4 ld16_cg(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st16(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+// Streaming store (evict-first): final outputs that nothing re-reads soon.
+__device__ __forceinline__ void st16_cs(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint8_t ld1_ro(const uint8_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return (uint8_t)v;
+}
+__device__ __forceinline__ uint8_t ld1_cg(const uint8_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+  return (uint8_t)v;
+}
+__device__ __forceinline__ void st1(uint8_t* p, uint8_t v) {
+  asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "h"((uint16_t)v) : "memory");
+}
+
+// Load policy: kRO for launch-constant inputs, kCG for data written in-launch.
+enum LoadKind { kRO = 0, kCG = 1 };
+// Store policy: plain, or streaming (evict-first) for final outputs.
+enum StoreKind { kST = 0, kCS = 1 };
+
+template <int LK>
+__device__ __forceinline__ uint4 ld16(const void* p) {
+  if (LK == kRO) return ld16_ro(p);
+  return ld16_cg(p);
+}
+template <int SK>
+__device__ __forceinline__ void st16k(void* p, uint4 v) {
+  if (SK == kCS)
+    st16_cs(p, v);
+  else
+    st16(p, v);
+}
+template <int LK>
+__device__ __forceinline__ uint8_t ld1(const uint8_t* p) {
+  if (LK == kRO) return ld1_ro(p);
+  return ld1_cg(p);
+}
+
+// Bytes m..m+15 (1 <= m <= 15) of the 32-byte little-endian concatenation a|b.
+__device__ __forceinline__ uint4 funnel16(uint4 a, uint4 b, unsigned m) {
+  uint64_t w0 = (uint64_t)a.x | ((uint64_t)a.y << 32);
+  uint64_t w1 = (uint64_t)a.z | ((uint64_t)a.w << 32);
+  uint64_t w2 = (uint64_t)b.x | ((uint64_t)b.y << 32);
+  if (m >= 8) {
+    w0 = w1;
+    w1 = w2;
+    w2 = (uint64_t)b.z | ((uint64_t)b.w << 32);
+    m -= 8;
+  }
+  uint64_t lo = w0, hi = w1;
+  if (m) {
+    const unsigned sh = m * 8;
+    lo = (w0 >> sh) | (w1 << (64 - sh));
+    hi = (w1 >> sh) | (w2 << (64 - sh));
+  }
+  return make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+}
+
+// ------------------------------------------------------- warp byte copy ---
+// One warp copies n bytes src -> dst (any alignments, non-overlapping).
+//  * head: bytes up to dst's next 16-byte boundary, one byte per lane;
+//  * body: 16-byte aligned stores; loads are 16-byte aligned too -- when src
+//    and dst disagree mod 16, each lane loads the aligned block under its
+//    output, takes the next block from its right neighbour by shuffle, and
+//    funnel-shifts the pair (a block read past the end of src stays inside
+//    src's 16-byte-aligned, 16-byte-padded allocation);
+//  * tail: the last < 16 bytes, one byte per lane.
+// U = 16-byte vectors in flight per lane.
+template <int U, int LK, int SK>
+__device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, size_t n, int lane) {
+  if (n == 0) return;
+  size_t head = (16 - ((uintptr_t)dst & 15)) & 15;
+  if (head > n) head = n;
+  if ((size_t)lane < head) st1(dst + lane, ld1<LK>(src + lane));
+  const size_t nvec = (n - head) >> 4;
+  uint8_t* d = dst + head;
+  const uint8_t* s = src + head;
+  const unsigned m = (unsigned)((uintptr_t)s & 15);
+  if (m == 0) {
+    size_t j = lane;
+    for (; j + 32 * (U - 1) < nvec; j += 32 * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = ld16<LK>(s + 16 * (j + 32 * u));
+#pragma unroll
+      for (int u = 0; u < U; ++u) st16k<SK>(d + 16 * (j + 32 * u), v[u]);
+    }
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (j + 32 * u < nvec) v[u] = ld16<LK>(s + 16 * (j + 32 * u));
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (j + 32 * u < nvec) st16k<SK>(d + 16 * (j + 32 * u), v[u]);
+  } else if (nvec) {
+    // aligned source blocks a[0..nvec] (nvec+1 of them) cover the body;
+    // half the vectors in flight of the aligned path (two blocks per output)
+    constexpr int V = U > 1 ? U / 2 : 1;
+    const uint8_t* a0 = s - m;
+    for (size_t base = 0; base < nvec; base += 32 * V) {  // warp-uniform loop
+      uint4 a[V];
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const size_t j = base + 32 * u + lane;
+        a[u] = j <= nvec ? ld16<LK>(a0 + 16 * j) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const size_t j = base + 32 * u + lane;
+        uint4 b;
+        b.x = __shfl_down_sync(0xffffffffu, a[u].x, 1);
+        b.y = __shfl_down_sync(0xffffffffu, a[u].y, 1);
+        b.z = __shfl_down_sync(0xffffffffu, a[u].z, 1);
+        b.w = __shfl_down_sync(0xffffffffu, a[u].w, 1);
+        if (lane == 31 && j + 1 <= nvec) b = ld16<LK>(a0 + 16 * (j + 1));
+        if (j < nvec) st16k<SK>(d + 16 * j, funnel16(a[u], b, m));
+      }
+    }
+  }
+  const size_t done = head + (nvec << 4);
+  if ((size_t)lane < n - done) st1(dst + done + lane, ld1<LK>(src + done + lane));
+}
+
+}  // namespace symm

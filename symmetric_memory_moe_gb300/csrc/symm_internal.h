@@ -1,0 +1,44 @@
+// symm_internal.h -- host-side state and helpers shared by the library's
+// translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/symm_a2a.h"
+
+struct symm_heap {
+  uint8_t* base;         // device; caller-owned
+  size_t slab;           // bytes per PE
+  int npes;              // W
+  size_t next;           // bump offset inside every slab
+  uint64_t spin_budget;  // ns
+  int device;            // CUDA device that was current at init
+  bool ctrl_ready;       // header zeroed on the device
+};
+
+namespace symm_host {
+
+// Records `msg` as this thread's last error and returns `code`.
+int fail(int code, const std::string& msg);
+// Maps a CUDA error to SYMM_ECUDA (with its name and `what`), or SYMM_OK.
+int cuda_check(cudaError_t e, const char* what);
+
+// Offset of `p` inside its slab when p lies in the heap, else -1.
+int64_t slab_offset(const symm_heap* h, const void* p);
+// Validates that [p, p + bytes) names a range of one slab past the header
+// and returns its slab offset in *off.
+int check_range(const symm_heap* h, const void* p, size_t bytes, const char* what, size_t* off);
+
+// Zeroes the header of slab 0 on `stream` the first time it is needed.
+int ensure_ctrl(symm_heap* h, cudaStream_t stream);
+
+// SMs of the current device, cached per device.
+int sm_count();
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace symm_host

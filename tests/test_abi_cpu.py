@@ -1,0 +1,133 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports
+every symbol include/symm_a2a.h declares, and its host-side logic (heap
+arithmetic, argument validation) behaves; no call here launches a kernel."""
+import os
+import re
+import subprocess
+
+import pytest
+
+from symmetric_memory_moe_gb300 import abi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "symm_a2a.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^(?:const\s+)?(?:int|void|char)\s*\**\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("symm_heap_init", "symm_malloc", "symm_at", "shmem_put", "shmem_get",
+                 "shmem_signal_op", "shmem_wait_for_signal", "shmem_put_with_signal",
+                 "all2all_dispatch", "all2all_combine", "all2all_combine_back"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    path = build.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    lib = abi.lib()
+    for n in declared_functions():
+        assert hasattr(lib, n)
+    assert set(declared_functions()) == set(abi._SIGS), "binding and header disagree"
+
+
+FAKE_BASE = 0x7F0000000000  # never dereferenced: host-only calls below
+
+
+def test_heap_arithmetic():
+    slab = 4 << 20
+    h = abi.symm_heap_init(FAKE_BASE, slab, 8)
+    try:
+        p = abi.symm_malloc(h, 1000)
+        assert p == FAKE_BASE + abi.SYMM_HEAP_HEADER_BYTES  # first allocation after the header
+        q = abi.symm_malloc(h, 10, 4096)
+        assert q % 4096 == 0 and q >= p + 1024  # previous one padded to 256
+        r = abi.symm_malloc(h, 1)
+        assert r % 256 == 0 and r == q + 256
+        # symm_at(p, pe) = base + pe*slab + (p - base) mod slab, from any slab
+        for pe in range(8):
+            assert abi.symm_at(h, p, pe) == FAKE_BASE + pe * slab + (p - FAKE_BASE)
+            assert abi.symm_at(h, abi.symm_at(h, q, 5), pe) == abi.symm_at(h, q, pe)
+        assert abi.symm_at(h, p, 8) is None and abi.symm_at(h, p, -1) is None
+        assert abi.symm_at(h, FAKE_BASE - 1, 0) is None
+        assert abi.symm_at(h, FAKE_BASE + 8 * slab, 0) is None
+        with pytest.raises(abi.SymmError) as e:
+            abi.symm_malloc(h, slab)
+        assert e.value.code == abi.SYMM_ENOMEM
+        with pytest.raises(abi.SymmError) as e:
+            abi.symm_malloc(h, 16, 3)
+        assert e.value.code == abi.SYMM_EINVAL
+        abi.symm_heap_reset(h)
+        assert abi.symm_malloc(h, 5) == p
+    finally:
+        abi.symm_heap_destroy(h)
+
+
+@pytest.mark.parametrize("base,slab,npes", [(FAKE_BASE + 16, 4 << 20, 2), (FAKE_BASE, 4096, 2),
+                                            (FAKE_BASE, (4 << 20) + 8, 2), (FAKE_BASE, 4 << 20, 0),
+                                            (0, 4 << 20, 2)])
+def test_heap_init_rejects(base, slab, npes):
+    with pytest.raises(abi.SymmError) as e:
+        abi.symm_heap_init(base, slab, npes)
+    assert e.value.code == abi.SYMM_EINVAL
+
+
+def test_pc_workspace_sizes():
+    # staging [buffer][tile_s][H*W][D], signals buffer*nbd*H*W slots of 64 B
+    st, sg = abi.all2all_pc_workspace(8, 2048, 1, 7168, 2, 16, 1792, 2)
+    assert st == 2 * 16 * 8 * 7168 * 2 and sg == 2 * 4 * 1 * 8 * 64
+    st, sg = abi.all2all_pc_workspace(32, 256, 2, 999, 2, 32, 0, 2)
+    assert st == 2 * 32 * 64 * 999 * 2 and sg == 2 * 1 * 2 * 32 * 64
+    with pytest.raises(abi.SymmError):
+        abi.all2all_pc_workspace(8, 16, 1, 8, 2, 0, 0, 2)
+
+
+def test_validation_happens_before_any_launch():
+    W, slab = 4, 8 << 20
+    h = abi.symm_heap_init(FAKE_BASE, slab, W)
+    try:
+        n = 16 * W * 2 * 8 * 2
+        a = abi.symm_malloc(h, n)
+        b = abi.symm_malloc(h, n)
+
+        def code(fn, *args):
+            with pytest.raises(abi.SymmError) as e:
+                fn(h, *args, stream=0)
+            return e.value.code
+
+        E = abi.SYMM_EINVAL
+        assert code(abi.all2all_combine, a, b, W + 1, 16, 2, 8, 2) == E       # W != npes
+        assert code(abi.all2all_combine, a, a, W, 16, 2, 8, 2) == E           # in == out
+        assert code(abi.all2all_combine, a, a + 64, W, 16, 2, 8, 2) == E      # overlap
+        assert code(abi.all2all_combine, a, b, W, 16, 2, 8, 0) == E           # elem_bytes 0
+        assert code(abi.all2all_combine, a, b, W, 16 << 10, 2, 8, 2) == E     # past the slab
+        assert code(abi.all2all_combine, FAKE_BASE, b, W, 16, 2, 8, 2) == E   # header
+        assert code(abi.all2all_combine, 0x1000, b, W, 16, 2, 8, 2) == E      # not in the heap
+        assert code(abi.all2all_combine, a, b, W, 16, 2, 8, 2, 7) == E        # bad variant
+        assert code(abi.all2all_dispatch, a, b, W, 18, 2, 8, 2) == E          # S % W
+        assert code(abi.all2all_combine_back, a, b, W, -1, 2, 8, 2) == E
+        # PC without (or with too small) workspace
+        assert code(abi.all2all_combine, a, b, W, 16, 2, 8, 2, abi.SYMM_A2A_PC, 4, 0, 2,
+                    None, None) == E
+        assert code(abi.all2all_combine, a, b, W, 16, 2, 8, 2, abi.SYMM_A2A_PC, 4, 0, 2,
+                    a, b) == E                                                  # overlaps in/out
+        # primitives
+        assert code(abi.shmem_put, a, 0, 0x1000, 0, 64, W) == E               # bad PE
+        assert code(abi.shmem_put, a, n, 0x1000, 0, slab, 0) == E             # past the slab
+        assert code(abi.shmem_get, 0x1000, 0, a, 0, 64, -1) == E
+        assert code(abi.shmem_signal_op, a, 0, 1, 2, 0) == E                  # op 2
+        assert code(abi.shmem_signal_op, a + 4, 0, 1, 0, 0) == E              # misaligned
+        assert code(abi.shmem_wait_for_signal, a, 0, 1, 3, 0) == E            # cmp 3
+        assert code(abi.shmem_put_with_signal, a, 0, 0x1000, 0, 64, b, 0, 1, 5, 0) == E
+    finally:
+        abi.symm_heap_destroy(h)

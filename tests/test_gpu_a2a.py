@@ -1,0 +1,218 @@
+"""GPU parity: the CUDA all-to-all through the C ABI against the CPU oracle.
+
+Results must be bit-exact (the path moves bits, it does no arithmetic).
+Outputs are poisoned (0xA5) before every call so an unwritten byte shows.
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from symmetric_memory_moe_gb300 import abi, inputs
+from symmetric_memory_moe_gb300.torch_heap import CombineBuffers
+
+pytestmark = pytest.mark.gpu
+
+POISON = 0xA5
+# producer/consumer D-block per workload: several blocks where D allows
+BLOCK_D = {"tiny": 0, "small": 64, "dsv3": 1792, "tail": 0}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.init()
+
+
+@functools.lru_cache(maxsize=2)
+def _workload_data(name):
+    wl = inputs.WORKLOADS[name]
+    x = inputs.make_input(wl)
+    return wl, x
+
+
+def _np_view(t: torch.Tensor) -> np.ndarray:
+    """Raw-bit numpy view of a CPU tensor (bf16 viewed as int16)."""
+    if t.dtype == torch.bfloat16:
+        t = t.view(torch.int16)
+    return t.numpy()
+
+
+def run_combine(x: torch.Tensor, W, S, H, D, variant, tile_s=16, block_d=0, buffer_num=2,
+                in_shift=0, out_shift=0, repeat=1):
+    """Runs all2all_combine on x ([W][S*W][H][D], CPU); returns [W, bytes] uint8."""
+    es = x.element_size()
+    pc = variant == "pc"
+    extra = 2048
+    bufs = CombineBuffers(W, S * W, H, D, es, pc=pc, S=S, tile_s=tile_s, block_d=block_d,
+                          buffer_num=buffer_num, extra=extra)
+    heap, n = bufs.heap, bufs.nbytes
+    inp, out = bufs.inp + in_shift, bufs.out + out_shift
+    heap.upload(inp, x.reshape(W, -1))
+    heap.views(out, n).fill_(POISON)
+    kind = abi.SYMM_A2A_PC if pc else abi.SYMM_A2A_DIRECT
+    for _ in range(repeat):
+        abi.all2all_combine(heap.handle, inp, out, W, S, H, D, es, kind, tile_s, block_d,
+                            buffer_num, bufs.staging, bufs.signals)
+    torch.cuda.synchronize()
+    rc, info = abi.symm_check_error(heap.handle)
+    assert rc == abi.SYMM_OK, (rc, info)
+    res = heap.download(out, n)
+    if pc:  # every slot returned to 0 by its consumer
+        sig = heap.download(bufs.signals, bufs.signal_bytes).view(torch.int64)
+        assert not sig.any()
+    heap.close()
+    return res
+
+
+def expect_combine(x, W, S, H, D):
+    y = oracle.load().combine(_np_view(x), W, S, H, D)
+    return y.view(np.uint8).reshape(W, -1)
+
+
+def assert_bits_equal(got: torch.Tensor, want: np.ndarray):
+    g = got.numpy()
+    if not np.array_equal(g, want):
+        bad = np.argwhere(g != want)
+        raise AssertionError(f"{len(bad)} bytes differ; first at (pe, byte) {bad[:5].tolist()}, "
+                             f"got {g[tuple(bad[0])]} want {want[tuple(bad[0])]}")
+
+
+# ------------------------------------------------ the five workloads ------
+@pytest.mark.parametrize("name,variant", [
+    ("tiny", "direct"), ("tiny", "pc"), ("small", "direct"), ("small", "pc"),
+    ("tail", "direct"), ("tail", "pc"), ("dsv3", "direct"), ("dsv3", "pc")])
+def test_workload_combine_bit_exact(name, variant):
+    wl, x = _workload_data(name)
+    got = run_combine(x, wl.W, wl.S, wl.H, wl.D, variant, tile_s=wl.tile_s,
+                      block_d=BLOCK_D[name])
+    assert_bits_equal(got, expect_combine(x, wl.W, wl.S, wl.H, wl.D))
+
+
+def test_tiny_golden_values():
+    """Hand-worked entries of the W=2 iota case, read off the GPU output."""
+    wl, x = _workload_data("tiny")
+    for variant in ("direct", "pc"):
+        got = run_combine(x, wl.W, wl.S, wl.H, wl.D, variant, tile_s=2).view(torch.int32)
+        got = got.reshape(wl.W, wl.S, wl.H * wl.W, wl.D)
+        assert got[0, 0, 2, 0] == 1000000 and got[0, 3, 1, 7] == 63
+        assert got[1, 0, 0, 0] == 64 and got[1, 3, 3, 7] == 1000127
+
+
+def test_roundtrip_dispatch_then_inverse():
+    """W=16 fp16 dispatch (1024,4,128) -> (64,64,128) matches the oracle, and
+    the inverse brings back the input bit for bit."""
+    wl, x = _workload_data("roundtrip")
+    W, S, H, D, es = wl.W, wl.S, wl.H, wl.D, wl.es
+    bufs = CombineBuffers(W, S, H, D, es, extra=S * H * D * es + 256)
+    heap, n = bufs.heap, bufs.nbytes
+    back = heap.malloc(n)
+    heap.upload(bufs.inp, x.reshape(W, -1))
+    heap.views(bufs.out, n).fill_(POISON)
+    heap.views(back, n).fill_(POISON)
+    abi.all2all_dispatch(heap.handle, bufs.inp, bufs.out, W, S, H, D, es)
+    abi.all2all_combine_back(heap.handle, bufs.out, back, W, S // W, H, D, es)
+    torch.cuda.synchronize()
+    want = oracle.load().dispatch(_np_view(x), W, S, H, D).view(np.uint8).reshape(W, -1)
+    assert_bits_equal(heap.download(bufs.out, n), want)
+    assert_bits_equal(heap.download(back, n), _np_view(x).view(np.uint8).reshape(W, -1))
+    heap.close()
+
+
+# ------------------------------------------------------------ edge cases --
+def _rand_bytes(W, rows, H, D, es, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(0, 256, (W, rows, H, D * es), generator=g, dtype=torch.uint8)
+
+
+@pytest.mark.parametrize("W,S,H,D,es,tile_s,block_d,buf", [
+    (1, 7, 3, 5, 2, 4, 0, 2),        # one PE: identity
+    (3, 37, 2, 999, 2, 16, 256, 2),   # odd W, ragged S and D blocks
+    (5, 9, 1, 33, 1, 4, 8, 3),        # bytes, 3 buffers
+    (4, 16, 2, 7, 3, 1, 0, 1),        # 3-byte elements, one row per tile, one buffer
+    (2, 5, 4, 16, 8, 2, 5, 2),        # 8-byte elements
+    (8, 12, 1, 1, 16, 5, 0, 2),       # 16-byte elements, one element per run
+    (6, 3, 3, 100, 4, 64, 17, 2),     # tile taller than S
+])
+@pytest.mark.parametrize("variant", ["direct", "pc"])
+def test_shapes(W, S, H, D, es, tile_s, block_d, buf, variant):
+    xe = _rand_bytes(W, S * W, H, D, es, seed=W * 1000 + S).reshape(W, S * W, H, D, es)
+    got = _run_es(xe, W, S, H, D, es, variant, tile_s, block_d, buf)
+    assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
+
+
+def _expect_es(xe, W, S, H, D, es):
+    """Oracle combine of raw es-byte elements (numpy void dtype)."""
+    xv = np.ascontiguousarray(xe.numpy()).view(np.dtype((np.void, es))).reshape(W, S * W, H, D)
+    return oracle.load().combine(xv, W, S, H, D).view(np.uint8).reshape(W, -1)
+
+
+def _run_es(xe, W, S, H, D, es, variant, tile_s, block_d, buf, in_shift=0, out_shift=0):
+    pc = variant == "pc"
+    bufs = CombineBuffers(W, S * W, H, D, es, pc=pc, S=S, tile_s=tile_s, block_d=block_d,
+                          buffer_num=buf, extra=2048)
+    heap, n = bufs.heap, bufs.nbytes
+    inp, out = bufs.inp + in_shift, bufs.out + out_shift
+    heap.upload(inp, xe.reshape(W, -1))
+    heap.views(out, n).fill_(POISON)
+    kind = abi.SYMM_A2A_PC if pc else abi.SYMM_A2A_DIRECT
+    abi.all2all_combine(heap.handle, inp, out, W, S, H, D, es, kind, tile_s, block_d, buf,
+                        bufs.staging, bufs.signals)
+    torch.cuda.synchronize()
+    assert abi.symm_check_error(heap.handle)[0] == abi.SYMM_OK
+    res = heap.download(out, n)
+    heap.close()
+    return res
+
+
+@pytest.mark.parametrize("in_shift,out_shift", [(2, 0), (0, 6), (3, 9), (14, 1), (16, 32)])
+@pytest.mark.parametrize("variant", ["direct", "pc"])
+def test_unaligned_base_pointers(in_shift, out_shift, variant):
+    """Input and output at arbitrary byte offsets: every src/dst phase mod 16."""
+    W, S, H, D, es = 4, 10, 2, 45, 2
+    xe = _rand_bytes(W, S * W, H, D, es, seed=in_shift * 31 + out_shift).reshape(W, S * W, H, D,
+                                                                                  es)
+    got = _run_es(xe, W, S, H, D, es, variant, 4, 16, 2, in_shift, out_shift)
+    assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
+
+
+@pytest.mark.parametrize("S,H,D", [(0, 2, 8), (4, 0, 8), (4, 2, 0)])
+def test_empty_extents_are_noops(S, H, D):
+    W = 2
+    bufs = CombineBuffers(W, 8, 2, 8, 2, pc=True, S=4, tile_s=2)
+    heap = bufs.heap
+    heap.views(bufs.out, 64).fill_(POISON)
+    for kind in (abi.SYMM_A2A_DIRECT, abi.SYMM_A2A_PC):
+        abi.all2all_combine(heap.handle, bufs.inp, bufs.out, W, S, H, D, 2, kind, 2, 0, 2,
+                            bufs.staging, bufs.signals)
+    abi.all2all_dispatch(heap.handle, bufs.inp, bufs.out, W, S, H, D, 2)
+    torch.cuda.synchronize()
+    assert (heap.download(bufs.out, 64) == POISON).all()
+    heap.close()
+
+
+def test_repeated_pc_calls_reuse_signals():
+    """Back-to-back PC launches on one workspace (reset in-stream each time)."""
+    W, S, H, D = 4, 24, 2, 40
+    x = _rand_bytes(W, S * W, H, D, 2, seed=5).view(torch.int16).reshape(W, S * W, H, D)
+    got = run_combine(x, W, S, H, D, "pc", tile_s=4, block_d=16, repeat=3)
+    assert_bits_equal(got, expect_combine(x, W, S, H, D))
+
+
+def test_host_buffer_entry_point():
+    """all2all_combine_host: host in -> device -> combine -> host out."""
+    W, S, H, D = 4, 16, 2, 24
+    x = _rand_bytes(W, S * W, H, D, 2, seed=9).view(torch.int16).reshape(W, S * W, H, D)
+    for variant, kind in (("direct", abi.SYMM_A2A_DIRECT), ("pc", abi.SYMM_A2A_PC)):
+        bufs = CombineBuffers(W, S * W, H, D, 2, pc=variant == "pc", S=S, tile_s=4)
+        host_in = x.contiguous().pin_memory()
+        host_out = torch.full((W, S, H * W, D), -1, dtype=torch.int16).pin_memory()
+        abi.all2all_combine_host(bufs.heap.handle, host_in.data_ptr(), host_out.data_ptr(),
+                                 bufs.inp, bufs.out, W, S, H, D, 2, kind, 4, 0, 2, bufs.staging,
+                                 bufs.signals)
+        torch.cuda.synchronize()
+        want = expect_combine(x, W, S, H, D)
+        assert np.array_equal(host_out.view(torch.uint8).reshape(W, -1).numpy(), want)
+        bufs.heap.close()
