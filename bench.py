@@ -30,7 +30,7 @@ METRIC = "reverse-All2All combine GB/s (read+write) and % of GB300 HBM roofline"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = "dsv3"
-PC_TILE_S, PC_BLOCK_D, PC_BUFFERS = 16, 1792, 2
+PC_TILE_S, PC_BLOCK_D, PC_BUFFERS = 16, 1024, 2
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 

@@ -19,12 +19,14 @@
 //    warp-specialised: warps 0-3 are a producer group, warps 4-7 a consumer
 //    group, each synchronised by its own named barrier.  The grid is capped at
 //    the CTAs that are resident at once, so every spin can be satisfied.
-//  * Tasks (S block b, destination d, source r, expert h, D block) are dealt
-//    to CTAs in one global order; a CTA's consumer group consumes exactly the
-//    tiles its own producer group staged, so a consumer never waits on a
-//    producer of another SM.  The page's target rotation (rank + i) % W
-//    staggers one PE's producers across destinations; here every (r, d) pair
-//    is in flight at once, so it has nothing left to stagger.
+//  * A task (destination d, source r, expert h, D block) is one signal slot;
+//    like the page's cores, each CTA owns a fixed set of tasks and walks the
+//    S blocks in order, its consumer group consuming exactly the tiles its own
+//    producer group staged.  Every wait is thus satisfied by the same CTA,
+//    and successive producers of a slot are ordered.  The page's target
+//    rotation (rank + i) % W staggers one PE's producers across
+//    destinations; here every (r, d) pair is in flight at once, so it has
+//    nothing left to stagger.
 //  * Copies move 16-byte vectors per lane (funnel-shifted when source and
 //    destination disagree mod 16) instead of masked 2-D tile loads; ragged
 //    S and D blocks are bounds in the row loop and the byte count.
@@ -102,12 +104,15 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks) a2a_pc_kernel(const 
   const int gtid = threadIdx.x & (kPcGroup - 1);
   const int bar_id = 1 + role;         // named barrier of the group
   const size_t tasks_per_block = (size_t)a.W * a.W * a.H * a.nbd;
-  const size_t total = (size_t)a.nbs * tasks_per_block;
   const size_t stage_row = (size_t)a.H * a.W * a.D * a.es;  // one staging row, bytes
 
-  for (size_t f = blockIdx.x; f < total; f += gridDim.x) {
-    const uint32_t b = (uint32_t)(f / tasks_per_block);
-    size_t q = f % tasks_per_block;  // q = ((d*W + r)*H + h)*nbd + bd
+  // As on the page, a task (one signal slot) belongs to one CTA for every S
+  // block and the CTA walks the S blocks in order: the producer of S block b
+  // and the consumer of S block b - buffer_num on the same slot are this
+  // CTA's own two groups, so no wait depends on another CTA.
+  for (uint32_t b = 0; b < a.nbs; ++b)
+  for (size_t q0 = blockIdx.x; q0 < tasks_per_block; q0 += gridDim.x) {
+    size_t q = q0;  // q = ((d*W + r)*H + h)*nbd + bd
     const uint32_t bd = (uint32_t)(q % a.nbd);
     q /= a.nbd;
     const uint32_t h = (uint32_t)(q % a.H);
@@ -306,10 +311,13 @@ static int combine_pc(symm_heap* h, size_t in_off, size_t out_off, size_t nbytes
   a.budget_ns = h->spin_budget;
   a.ctl = reinterpret_cast<Control*>(h->base);
   a.heap_base = h->base;
-  const size_t tasks = (size_t)a.nbs * W * W * H * nbd;
+  // tasks of one S block, dealt evenly: k per CTA, ceil(tasks / k) CTAs, never
+  // more CTAs than are resident at once
+  const size_t tasks = (size_t)W * W * H * nbd;
   int cap = resident_ctas((const void*)a2a_pc_kernel, kPcThreads);
   if (cap <= 0) return fail(SYMM_ECUDA, "all2all_combine: occupancy query failed");
-  const int grid = (int)(tasks < (size_t)cap ? tasks : (size_t)cap);
+  const size_t per_cta = (tasks + cap - 1) / cap;
+  const int grid = (int)((tasks + per_cta - 1) / per_cta);
   a2a_pc_kernel<<<grid, kPcThreads, 0, s>>>(a);
   return cuda_check(cudaGetLastError(), "all2all_combine: PC launch");
 }
