@@ -217,6 +217,38 @@ int all2all_combine_host(symm_heap_t *heap, const void *host_in, void *host_out,
                          int tile_s, int block_d, int buffer_num, void *staging, int64_t *signals,
                          void *stream);
 
+/* ------------------------------------------- allocation-free variant -- */
+
+/* Size of the library's own static device array used by
+ * all2all_combine_pc_noalloc (32 MiB, held on every GPU that loads the
+ * library until the process exits). */
+#define SYMM_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* No counterpart on the pages: an addition for callers that cannot allocate
+ * device memory -- code whose device memory is all handed out beforehand by
+ * another allocator, or a hot path that must not pay the device-wide
+ * synchronisation of cudaMalloc/cudaFree -- but still want the staged,
+ * signalled combine.  Same operation and arguments as
+ * all2all_combine(SYMM_A2A_PC) except that the staging ring and the signal
+ * slots live in the library's static SYMM_NOALLOC_SCRATCH_BYTES array
+ * instead of the caller's heap; the caller passes only the symmetric input
+ * and output.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - Needs W * (roundup256(buffer_num*tile_s*H*W*D*elem_bytes) +
+ *    roundup256(buffer_num*W*nbd*H*64)) bytes of scratch; larger requests
+ *    return SYMM_EINVAL before launching anything.
+ *  - Each call zeroes its signal slots in the array first (the array keeps
+ *    the last call's contents).  All calls share the one array per device:
+ *    calls that overlap on the GPU (other streams, other threads, other
+ *    heaps) race and give undefined output; order them on one stream.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ * Errors: SYMM_EINVAL, SYMM_ECUDA; a wait that gives up shows in
+ * symm_check_error(). */
+int all2all_combine_pc_noalloc(symm_heap_t *heap, const void *in, void *out, int W, int S, int H,
+                               int D, int elem_bytes, int tile_s, int block_d, int buffer_num,
+                               void *stream);
+
 #ifdef __cplusplus
 }
 #endif

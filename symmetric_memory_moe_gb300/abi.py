@@ -29,6 +29,7 @@ SYMM_A2A_PC = 1
 SYMM_A2A_FLAG_NO_RESET = 0x100
 SYMM_HEAP_HEADER_BYTES = 4096
 SYMM_SIGNAL_STRIDE_BYTES = 64
+SYMM_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _NAMES = {SYMM_EINVAL: "SYMM_EINVAL", SYMM_ENOMEM: "SYMM_ENOMEM",
           SYMM_ETIMEDOUT: "SYMM_ETIMEDOUT", SYMM_ECUDA: "SYMM_ECUDA"}
@@ -66,6 +67,7 @@ _SIGS = {
     "all2all_dispatch": [_P, _P, _P, _I, _I, _I, _I, _I, _P],
     "all2all_combine_back": [_P, _P, _P, _I, _I, _I, _I, _I, _P],
     "all2all_combine_host": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P],
+    "all2all_combine_pc_noalloc": [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
 }
 
 _lock = threading.Lock()
@@ -219,3 +221,13 @@ def all2all_combine_host(heap, host_in, host_out, inp, out, W, S, H, D, elem_byt
     _check(lib().all2all_combine_host(heap, host_in, host_out, inp, out, W, S, H, D, elem_bytes,
                                       variant, tile_s, block_d, buffer_num, staging, signals,
                                       _stream(stream)), "all2all_combine_host")
+
+
+def all2all_combine_pc_noalloc(heap, inp, out, W, S, H, D, elem_bytes, tile_s=16, block_d=0,
+                               buffer_num=2, stream=None):
+    """The producer/consumer combine with its staging and signals in the
+    library's static scratch array, for callers that cannot allocate device
+    memory; see include/symm_a2a.h."""
+    _check(lib().all2all_combine_pc_noalloc(heap, inp, out, W, S, H, D, elem_bytes, tile_s,
+                                            block_d, buffer_num, _stream(stream)),
+           "all2all_combine_pc_noalloc")
