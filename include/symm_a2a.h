@@ -57,6 +57,10 @@ extern "C" {
 /* OR-ed into the variant: skip the signal reset that precedes a PC launch
  * (the caller has zeroed the signal slots itself) */
 #define SYMM_A2A_FLAG_NO_RESET 0x100
+/* OR-ed into the variant: move data with 16-byte vector loads/stores even
+ * where bulk (TMA) copies through shared memory apply.  By default a launch
+ * whose rows are all 16-byte aligned uses bulk copies. */
+#define SYMM_A2A_FLAG_VECTOR 0x200
 
 /* bytes at the start of every slab that the heap keeps for itself */
 #define SYMM_HEAP_HEADER_BYTES 4096

@@ -27,6 +27,7 @@ SYMM_CMP_LT = 2
 SYMM_A2A_DIRECT = 0
 SYMM_A2A_PC = 1
 SYMM_A2A_FLAG_NO_RESET = 0x100
+SYMM_A2A_FLAG_VECTOR = 0x200
 SYMM_HEAP_HEADER_BYTES = 4096
 SYMM_SIGNAL_STRIDE_BYTES = 64
 SYMM_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -75,15 +76,16 @@ _lib = None
 
 
 def lib_path() -> str:
-    return _build.LIB_PATH
+    return os.environ.get("SYMM_A2A_LIB") or _build.LIB_PATH
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded library (built with nvcc first if it is missing or stale)."""
+    """The loaded library: $SYMM_A2A_LIB if set (a prebuilt libsymm_a2a.so),
+    else the in-tree build (compiled with nvcc first if missing or stale)."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
+            path = os.environ.get("SYMM_A2A_LIB") or _build.build()
             if not os.path.exists(path):
                 raise ImportError(f"libsymm_a2a.so missing at {path}")
             cdll = ctypes.CDLL(path)

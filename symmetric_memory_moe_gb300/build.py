@@ -44,19 +44,24 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of libsymm_a2a.so."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, defines: tuple = (),
+          out: str | None = None) -> str:
+    """Compile (if stale) and return the path of libsymm_a2a.so.  `defines`
+    (e.g. ("SYMM_PC_UNROLL=8",)) and `out` build a tuning variant elsewhere."""
+    if out is None and not defines and not force and up_to_date():
         return LIB_PATH
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    lib_path = out or LIB_PATH
+    build_dir = os.path.dirname(lib_path) if out else BUILD_DIR
+    os.makedirs(build_dir, exist_ok=True)
+    dflags = [f"-D{d}" for d in defines]
 
     def compile_one(src: str) -> str:
         name = os.path.splitext(src)[0]
-        obj = os.path.join(BUILD_DIR, name + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(build_dir, name + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *dflags, "-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
-        with open(os.path.join(BUILD_DIR, f"ptxas_{name}.log"), "w") as f:
+        with open(os.path.join(build_dir, f"ptxas_{name}.log"), "w") as f:
             f.write(res.stdout + res.stderr)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{res.stderr[-4000:]}")
@@ -66,13 +71,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{res.stderr[-4000:]}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

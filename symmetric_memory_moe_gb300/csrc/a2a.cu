@@ -47,10 +47,25 @@ using namespace symm_host;
 
 namespace {
 
+// Tuning knobs (compile-time): 16-byte vectors in flight per lane, and the
+// minimum resident CTAs per SM that register allocation must allow.
+#ifndef SYMM_RUNS_UNROLL
+#define SYMM_RUNS_UNROLL 4
+#endif
+#ifndef SYMM_RUNS_MIN_BLOCKS
+#define SYMM_RUNS_MIN_BLOCKS 1
+#endif
+#ifndef SYMM_PC_UNROLL
+#define SYMM_PC_UNROLL 4
+#endif
+#ifndef SYMM_PC_MIN_BLOCKS
+#define SYMM_PC_MIN_BLOCKS 3
+#endif
+
 constexpr int kRunThreads = 256;
 constexpr int kPcThreads = 256;  // 4 producer warps + 4 consumer warps
 constexpr int kPcGroup = 128;
-constexpr int kPcMinBlocks = 3;
+constexpr int kPcMinBlocks = SYMM_PC_MIN_BLOCKS;
 
 // --------------------------------------------------------------- direct ---
 // One warp per run of R = H*D*elem_bytes contiguous bytes, destination-major.
@@ -60,7 +75,7 @@ constexpr int kPcMinBlocks = 3;
 //   run k = (r*W + d)*Sb + s : in slab d row s*W + r   ->  out slab r row d*Sb + s
 // (a "row" here is one run of R bytes).
 template <bool INVERSE>
-__global__ void __launch_bounds__(kRunThreads)
+__global__ void __launch_bounds__(kRunThreads, SYMM_RUNS_MIN_BLOCKS)
     a2a_runs_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, size_t slab,
                     uint32_t W, uint32_t Sb, size_t R, uint32_t nruns) {
   const int lane = threadIdx.x & 31;
@@ -78,8 +93,92 @@ __global__ void __launch_bounds__(kRunThreads)
       src = in + d * slab + (size_t)(s * W + r) * R;
       dst = out + r * slab + (size_t)(d * Sb + s) * R;
     }
-    symm::warp_copy<4, symm::kRO, symm::kCS>(dst, src, R, lane);
+    symm::warp_copy<SYMM_RUNS_UNROLL, symm::kRO, symm::kCS>(dst, src, R, lane);
   }
+}
+
+// ------------------------------------------------------ direct, bulk ---
+// The same run permutation moved by the Tensor Memory Accelerator: one thread
+// per CTA streams units (runs cut into <= kBulkChunk-byte pieces) through a
+// ring of kBulkStages shared-memory buffers -- a bulk load global->shared
+// completing on the stage's mbarrier, then a bulk store shared->global --
+// keeping kBulkStages loads in flight without holding data in registers.
+// Needs 16-byte-aligned runs (R % 16 == 0, 16-byte-aligned bases).
+#ifndef SYMM_BULK_STAGES
+#define SYMM_BULK_STAGES 4
+#endif
+#ifndef SYMM_BULK_CHUNK
+#define SYMM_BULK_CHUNK 16384
+#endif
+constexpr int kBulkStages = SYMM_BULK_STAGES;
+constexpr uint32_t kBulkChunk = SYMM_BULK_CHUNK;
+constexpr size_t kBulkSmem = 128 + (size_t)kBulkStages * kBulkChunk;
+
+template <bool INVERSE>
+__device__ __forceinline__ void run_unit(const uint8_t* in, uint8_t* out, size_t slab, uint32_t W,
+                                         uint32_t Sb, size_t R, uint32_t nchunks, uint64_t u,
+                                         const uint8_t** src, uint8_t** dst, uint32_t* len) {
+  const uint32_t k = (uint32_t)(u / nchunks), c = (uint32_t)(u % nchunks);
+  const size_t off = (size_t)c * kBulkChunk;
+  if (!INVERSE) {
+    const uint32_t r = k % W, t = k / W, s = t % Sb, d = t / Sb;
+    *src = in + r * slab + (size_t)(d * Sb + s) * R + off;
+    *dst = out + d * slab + (size_t)(s * W + r) * R + off;
+  } else {
+    const uint32_t s = k % Sb, t = k / Sb, d = t % W, r = t / W;
+    *src = in + d * slab + (size_t)(s * W + r) * R + off;
+    *dst = out + r * slab + (size_t)(d * Sb + s) * R + off;
+  }
+  *len = (uint32_t)(R - off < kBulkChunk ? R - off : kBulkChunk);
+}
+
+template <bool INVERSE>
+__global__ void __launch_bounds__(32)
+    a2a_runs_bulk_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, size_t slab,
+                         uint32_t W, uint32_t Sb, size_t R, uint32_t nruns, uint32_t nchunks,
+                         uint64_t budget_ns, Control* ctl) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+  uint8_t* buf = smem + 128;
+  if (threadIdx.x != 0) return;
+  for (int st = 0; st < kBulkStages; ++st) symm::mbar_init(&bar[st], 1);
+  symm::fence_mbar_init();
+  const uint64_t units = (uint64_t)nruns * nchunks;
+  const uint64_t mine = units > blockIdx.x ? (units - blockIdx.x - 1) / gridDim.x + 1 : 0;
+  const uint8_t* src;
+  uint8_t* dst;
+  uint32_t len;
+  uint64_t issued = 0;
+  for (; issued < mine && issued < (uint64_t)kBulkStages; ++issued) {
+    run_unit<INVERSE>(in, out, slab, W, Sb, R, nchunks, blockIdx.x + issued * gridDim.x, &src,
+                      &dst, &len);
+    symm::mbar_arrive_expect_tx(&bar[issued], len);
+    symm::bulk_load(buf + issued * kBulkChunk, src, len, &bar[issued]);
+  }
+  uint64_t i = 0;
+  for (; i < mine; ++i) {
+    const int st = (int)(i % kBulkStages);
+    if (!symm::mbar_wait(&bar[st], (uint32_t)(i / kBulkStages) & 1u, budget_ns)) {
+      symm::record_error(ctl, symm::kErrTimedOut, -1);
+      break;
+    }
+    run_unit<INVERSE>(in, out, slab, W, Sb, R, nchunks, blockIdx.x + i * gridDim.x, &src, &dst,
+                      &len);
+    symm::bulk_store(dst, buf + (size_t)st * kBulkChunk, len);
+    symm::bulk_commit();
+    if (issued < mine) {  // refill this stage once the store has read it
+      symm::bulk_wait_read<0>();
+      run_unit<INVERSE>(in, out, slab, W, Sb, R, nchunks, blockIdx.x + issued * gridDim.x, &src,
+                        &dst, &len);
+      symm::mbar_arrive_expect_tx(&bar[st], len);
+      symm::bulk_load(buf + (size_t)st * kBulkChunk, src, len, &bar[st]);
+      ++issued;
+    }
+  }
+  // after a give-up, let the loads still in flight land (again bounded)
+  for (; i < issued; ++i)
+    symm::mbar_wait(&bar[i % kBulkStages], (uint32_t)(i / kBulkStages) & 1u, budget_ns);
+  symm::bulk_wait<0>();
 }
 
 // ------------------------------------------------ producer / consumer ---
@@ -96,7 +195,55 @@ struct PcArgs {
   const uint8_t* heap_base;
 };
 
-__global__ void __launch_bounds__(kPcThreads, kPcMinBlocks) a2a_pc_kernel(const PcArgs a) {
+// Input rows of one producer task (tile of S block b, slot q), for the
+// bulk prefetch: q = blockIdx.x + j*gridDim.x is the CTA's j-th slot.
+struct PcTile {
+  const uint8_t* src;  // input row 0 (source PE r)
+  uint32_t rows, len;
+};
+
+__device__ __forceinline__ PcTile pc_tile(const PcArgs& a, uint32_t nq, uint64_t t) {
+  const uint32_t b = (uint32_t)(t / nq);
+  size_t q = blockIdx.x + (size_t)(t % nq) * gridDim.x;  // q = ((d*W + r)*H + h)*nbd + bd
+  const uint32_t bd = (uint32_t)(q % a.nbd);
+  q /= a.nbd;
+  const uint32_t h = (uint32_t)(q % a.H);
+  q /= a.H;
+  const uint32_t r = (uint32_t)(q % a.W);
+  const uint32_t d = (uint32_t)(q / a.W);
+  const uint32_t s0 = b * a.tile_s, x0 = bd * a.block_d;
+  PcTile k;
+  k.src = a.in + r * a.slab + (((size_t)(d * a.S + s0) * a.H + h) * a.D + x0) * a.es;
+  k.rows = min(a.tile_s, a.S - s0);
+  k.len = min(a.block_d, a.D - x0) * a.es;
+  return k;
+}
+
+// Issues the bulk loads of task t's input tile into `tile` (one mbarrier phase).
+__device__ __forceinline__ void pc_prefetch(const PcArgs& a, uint32_t nq, uint64_t t,
+                                            uint8_t* tile, uint64_t* bar) {
+  const PcTile k = pc_tile(a, nq, t);
+  const size_t src_row = (size_t)a.H * a.D * a.es;
+  symm::mbar_arrive_expect_tx(bar, k.rows * k.len);
+  for (uint32_t i = 0; i < k.rows; ++i)
+    symm::bulk_load(tile + i * k.len, k.src + i * src_row, k.len, bar);
+}
+
+// PREFETCH: the producer group's thread 0 keeps the input tiles of the next
+// kPcPrefetch tasks in flight with bulk (TMA) loads into a shared-memory
+// ring, so producer warps only copy shared memory -> staging (16-byte
+// vectors); needs 16-byte-aligned tile rows.  Without it, producer warps
+// load the input with 16-byte vectors themselves.
+#ifndef SYMM_PC_PREFETCH
+#define SYMM_PC_PREFETCH 2
+#endif
+constexpr int kPcPrefetch = SYMM_PC_PREFETCH;
+constexpr uint32_t kPcMaxPrefetchTile = 32 * 1024;
+
+template <bool PREFETCH>
+__global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
+    a2a_pc_kernel(const PcArgs a, uint32_t tile_bytes) {
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int status[2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int role = warp >> 2;          // 0 = producer group, 1 = consumer group
@@ -105,13 +252,28 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks) a2a_pc_kernel(const 
   const int bar_id = 1 + role;         // named barrier of the group
   const size_t tasks_per_block = (size_t)a.W * a.W * a.H * a.nbd;
   const size_t stage_row = (size_t)a.H * a.W * a.D * a.es;  // one staging row, bytes
+  const uint32_t nq = (uint32_t)((tasks_per_block - blockIdx.x - 1) / gridDim.x + 1);
+  const uint64_t ntasks = (uint64_t)a.nbs * nq;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint8_t* ring = smem + 128;
+  uint64_t issued = 0;
+  if (PREFETCH && role == 0) {
+    if (gtid == 0) {
+      for (int i = 0; i < kPcPrefetch; ++i) symm::mbar_init(&bars[i], 1);
+      symm::fence_mbar_init();
+      for (; issued < ntasks && issued < (uint64_t)kPcPrefetch; ++issued)
+        pc_prefetch(a, nq, issued, ring + issued * tile_bytes, &bars[issued]);
+    }
+    symm::group_sync(bar_id, kPcGroup);
+  }
 
   // As on the page, a task (one signal slot) belongs to one CTA for every S
   // block and the CTA walks the S blocks in order: the producer of S block b
   // and the consumer of S block b - buffer_num on the same slot are this
   // CTA's own two groups, so no wait depends on another CTA.
+  uint64_t t = 0;
   for (uint32_t b = 0; b < a.nbs; ++b)
-  for (size_t q0 = blockIdx.x; q0 < tasks_per_block; q0 += gridDim.x) {
+  for (size_t q0 = blockIdx.x; q0 < tasks_per_block; q0 += gridDim.x, ++t) {
     size_t q = q0;  // q = ((d*W + r)*H + h)*nbd + bd
     const uint32_t bd = (uint32_t)(q % a.nbd);
     q /= a.nbd;
@@ -130,30 +292,65 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks) a2a_pc_kernel(const 
     const size_t len = (size_t)min(a.block_d, a.D - x0) * a.es;
     const size_t stage_col = ((size_t)(r * a.H + h) * a.D + x0) * a.es;
     uint8_t* stage = a.staging + d * a.slab + (size_t)buf * a.tile_s * stage_row + stage_col;
+    const int st = (int)(t % kPcPrefetch);
 
-    if (gtid == 0)
-      status[role] =
-          symm::spin_wait(slot, symm::kCmpEq, role == 0 ? 0 : 1, a.budget_ns, a.ctl, a.heap_base);
+    if (gtid == 0) {
+      int rc = symm::kSpinOk;
+      if (PREFETCH && role == 0 &&
+          !symm::mbar_wait(&bars[st], (uint32_t)(t / kPcPrefetch) & 1u, a.budget_ns)) {
+        symm::record_error(a.ctl, symm::kErrTimedOut, -1);
+        rc = symm::kSpinTimeout;
+      }
+      if (rc == symm::kSpinOk)
+        rc = symm::spin_wait(slot, symm::kCmpEq, role == 0 ? 0 : 1, a.budget_ns, a.ctl,
+                             a.heap_base);
+      status[role] = rc;
+    }
     symm::group_sync(bar_id, kPcGroup);
-    if (status[role] != symm::kSpinOk) return;  // uniform across the group
+    if (status[role] != symm::kSpinOk) {
+      // let this group's prefetches still in flight land (bounded), then leave
+      if (PREFETCH && role == 0 && gtid == 0)
+        for (uint64_t i = t; i < issued; ++i)
+          symm::mbar_wait(&bars[i % kPcPrefetch], (uint32_t)(i / kPcPrefetch) & 1u, a.budget_ns);
+      return;  // uniform across the group
+    }
 
     if (role == 0) {
-      // producer: input rows d*S + s0 + i of source r -> destination d's slot
-      const uint8_t* src =
-          a.in + r * a.slab + (((size_t)(d * a.S + s0) * a.H + h) * a.D + x0) * a.es;
-      const size_t src_row = (size_t)a.H * a.D * a.es;
-      for (uint32_t i = gwarp; i < rows; i += 4)
-        symm::warp_copy<4, symm::kRO, symm::kST>(stage + i * stage_row, src + i * src_row, len,
-                                                  lane);
+      if (PREFETCH) {
+        // shared-memory tile -> destination d's slot, 16 bytes per thread-step
+        const uint8_t* tile = ring + (size_t)st * tile_bytes;
+        const uint32_t vrow = (uint32_t)(len >> 4), nv = rows * vrow;
+        for (uint32_t v = gtid; v < nv; v += kPcGroup) {
+          const uint32_t i = v / vrow, c = v - i * vrow;
+          symm::st16(stage + i * stage_row + 16 * c,
+                     *reinterpret_cast<const uint4*>(tile + i * len + 16 * c));
+        }
+      } else {
+        // producer: input rows d*S + s0 + i of source r -> destination d's slot
+        const uint8_t* src =
+            a.in + r * a.slab + (((size_t)(d * a.S + s0) * a.H + h) * a.D + x0) * a.es;
+        const size_t src_row = (size_t)a.H * a.D * a.es;
+        for (uint32_t i = gwarp; i < rows; i += 4)
+          symm::warp_copy<SYMM_PC_UNROLL, symm::kRO, symm::kST>(stage + i * stage_row,
+                                                                 src + i * src_row, len, lane);
+      }
     } else {
       // consumer: staged tile -> output rows s0 + i, column r*H + h
       uint8_t* dst = a.out + d * a.slab + ((size_t)s0 * a.H * a.W * a.D) * a.es + stage_col;
       for (uint32_t i = gwarp; i < rows; i += 4)
-        symm::warp_copy<4, symm::kCG, symm::kCS>(dst + i * stage_row, stage + i * stage_row, len,
-                                                  lane);
+        symm::warp_copy<SYMM_PC_UNROLL, symm::kCG, symm::kCS>(dst + i * stage_row,
+                                                               stage + i * stage_row, len, lane);
     }
     symm::group_sync(bar_id, kPcGroup);  // the group's copies precede the release
-    if (gtid == 0) symm::st_release(slot, role == 0 ? 1 : 0);
+    if (gtid == 0) {
+      symm::st_release(slot, role == 0 ? 1 : 0);
+      if (PREFETCH && role == 0 && issued < ntasks) {
+        // every producer thread has read this ring slot: refill it
+        symm::fence_proxy_async_shared();
+        pc_prefetch(a, nq, issued, ring + (size_t)st * tile_bytes, &bars[st]);
+        ++issued;
+      }
+    }
   }
 }
 
@@ -169,21 +366,27 @@ __global__ void a2a_signal_reset_kernel(uint8_t* signals, size_t slab, uint32_t 
 }
 
 // ------------------------------------------------------------ launching ---
-// CTAs of `kernel` (launched with `threads` threads, no dynamic shared
-// memory) that are resident on the current device at once; cached.
-int resident_ctas(const void* kernel, int threads) {
+// CTAs of `kernel` (launched with `threads` threads and `smem` bytes of
+// dynamic shared memory) that are resident on the current device at once;
+// cached.  Raises the kernel's dynamic shared memory limit first if needed.
+int resident_ctas(const void* kernel, int threads, size_t smem = 0, size_t smem_limit = 0) {
   static std::mutex mu;
-  static std::map<std::pair<int, const void*>, int> cache;
+  static std::map<std::pair<std::pair<int, const void*>, size_t>, int> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find({dev, kernel});
+  auto it = cache.find({{dev, kernel}, smem});
   if (it != cache.end()) return it->second;
+  if (smem_limit < smem) smem_limit = smem;
+  if (smem_limit > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_limit) != cudaSuccess)
+    return 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess)
     return 0;
   const int n = per_sm * sm_count();
-  cache[{dev, kernel}] = n;
+  cache[{{dev, kernel}, smem}] = n;
   return n;
 }
 
@@ -217,19 +420,43 @@ int check_perm(symm_heap* h, const void* in, const void* out, int W, size_t rows
   return SYMM_OK;
 }
 
+// Launches the run permutation; bulk (TMA) copies when every run is 16-byte
+// aligned and `vector_only` is false, 16-byte vector loads/stores otherwise.
 int launch_runs(symm_heap* h, size_t in_off, size_t out_off, uint32_t W, uint32_t Sb, size_t R,
-                bool inverse, cudaStream_t s, const char* what) {
+                bool inverse, bool vector_only, cudaStream_t s, const char* what) {
   const size_t nruns = (size_t)W * W * Sb;
   if (nruns == 0 || R == 0) return SYMM_OK;
   if (nruns > 0x7fffffffull)
     return fail(SYMM_EINVAL, std::string(what) + ": more than 2^31 runs");
+  const uint8_t* in = h->base + in_off;
+  uint8_t* out = h->base + out_off;
+  const bool bulk = !vector_only && R % 16 == 0 && in_off % 16 == 0 && out_off % 16 == 0;
+  if (bulk) {
+    int rc = ensure_ctrl(h, s);
+    if (rc) return rc;
+    const void* kfn = inverse ? (const void*)a2a_runs_bulk_kernel<true>
+                              : (const void*)a2a_runs_bulk_kernel<false>;
+    const int cap = resident_ctas(kfn, 32, kBulkSmem);
+    if (cap <= 0) return fail(SYMM_ECUDA, std::string(what) + ": bulk kernel set-up failed");
+    const uint32_t nchunks = (uint32_t)((R + kBulkChunk - 1) / kBulkChunk);
+    const uint64_t units = (uint64_t)nruns * nchunks;
+    const int grid = (int)(units < (uint64_t)cap ? units : (uint64_t)cap);
+    Control* ctl = reinterpret_cast<Control*>(h->base);
+    if (inverse)
+      a2a_runs_bulk_kernel<true><<<grid, 32, kBulkSmem, s>>>(in, out, h->slab, W, Sb, R,
+                                                             (uint32_t)nruns, nchunks,
+                                                             h->spin_budget, ctl);
+    else
+      a2a_runs_bulk_kernel<false><<<grid, 32, kBulkSmem, s>>>(in, out, h->slab, W, Sb, R,
+                                                              (uint32_t)nruns, nchunks,
+                                                              h->spin_budget, ctl);
+    return cuda_check(cudaGetLastError(), what);
+  }
   const void* kfn = inverse ? (const void*)a2a_runs_kernel<true> : (const void*)a2a_runs_kernel<false>;
   int cap = resident_ctas(kfn, kRunThreads);
   if (cap <= 0) cap = 4 * (sm_count() > 0 ? sm_count() : 1);
   const size_t need = (nruns + kRunThreads / 32 - 1) / (kRunThreads / 32);
   const int grid = (int)(need < (size_t)cap ? need : (size_t)cap);
-  const uint8_t* in = h->base + in_off;
-  uint8_t* out = h->base + out_off;
   if (inverse)
     a2a_runs_kernel<true><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R, (uint32_t)nruns);
   else
@@ -314,11 +541,23 @@ static int combine_pc(symm_heap* h, size_t in_off, size_t out_off, size_t nbytes
   // tasks of one S block, dealt evenly: k per CTA, ceil(tasks / k) CTAs, never
   // more CTAs than are resident at once
   const size_t tasks = (size_t)W * W * H * nbd;
-  int cap = resident_ctas((const void*)a2a_pc_kernel, kPcThreads);
+  // input prefetch by bulk copies when every tile row is 16-byte aligned and a
+  // tile fits the shared-memory ring
+  const size_t tile_bytes = (size_t)tile_s * bd * es;
+  const bool prefetch = !(flags & SYMM_A2A_FLAG_VECTOR) && ((size_t)D * es) % 16 == 0 &&
+                        ((size_t)bd * es) % 16 == 0 && in_off % 16 == 0 &&
+                        tile_bytes <= kPcMaxPrefetchTile;
+  const void* kfn = prefetch ? (const void*)a2a_pc_kernel<true> : (const void*)a2a_pc_kernel<false>;
+  const size_t smem = prefetch ? 128 + (size_t)kPcPrefetch * tile_bytes : 0;
+  const int cap = resident_ctas(kfn, kPcThreads, smem,
+                                prefetch ? 128 + (size_t)kPcPrefetch * kPcMaxPrefetchTile : 0);
   if (cap <= 0) return fail(SYMM_ECUDA, "all2all_combine: occupancy query failed");
   const size_t per_cta = (tasks + cap - 1) / cap;
   const int grid = (int)((tasks + per_cta - 1) / per_cta);
-  a2a_pc_kernel<<<grid, kPcThreads, 0, s>>>(a);
+  if (prefetch)
+    a2a_pc_kernel<true><<<grid, kPcThreads, smem, s>>>(a, (uint32_t)tile_bytes);
+  else
+    a2a_pc_kernel<false><<<grid, kPcThreads, 0, s>>>(a, 0u);
   return cuda_check(cudaGetLastError(), "all2all_combine: PC launch");
 }
 
@@ -331,11 +570,12 @@ extern "C" int all2all_combine(symm_heap_t* h, const void* in, void* out, int W,
                       &out_off, &nbytes);
   if (rc) return rc;
   const int kind = variant & 0xff, flags = variant & ~0xff;
-  if (flags & ~SYMM_A2A_FLAG_NO_RESET) return fail(SYMM_EINVAL, "all2all_combine: unknown flag");
+  if (flags & ~(SYMM_A2A_FLAG_NO_RESET | SYMM_A2A_FLAG_VECTOR))
+    return fail(SYMM_EINVAL, "all2all_combine: unknown flag");
   cudaStream_t s = as_stream(stream);
   if (kind == SYMM_A2A_DIRECT)
-    return launch_runs(h, in_off, out_off, W, S, (size_t)H * D * elem_bytes, false, s,
-                       "all2all_combine");
+    return launch_runs(h, in_off, out_off, W, S, (size_t)H * D * elem_bytes, false,
+                       (flags & SYMM_A2A_FLAG_VECTOR) != 0, s, "all2all_combine");
   if (kind == SYMM_A2A_PC)
     return combine_pc(h, in_off, out_off, nbytes, W, S, H, D, elem_bytes, flags, tile_s, block_d,
                       buffer_num, staging, signals, s);
@@ -350,7 +590,7 @@ extern "C" int all2all_dispatch(symm_heap_t* h, const void* in, void* out, int W
   int rc = check_perm(h, in, out, W, (size_t)S, H, D, elem_bytes, "all2all_dispatch", &in_off,
                       &out_off, &nbytes);
   if (rc) return rc;
-  return launch_runs(h, in_off, out_off, W, S / W, (size_t)H * D * elem_bytes, false,
+  return launch_runs(h, in_off, out_off, W, S / W, (size_t)H * D * elem_bytes, false, false,
                      as_stream(stream), "all2all_dispatch");
 }
 
@@ -361,7 +601,7 @@ extern "C" int all2all_combine_back(symm_heap_t* h, const void* in, void* out, i
   int rc = check_perm(h, in, out, W, (size_t)Sp * W, H, D, elem_bytes, "all2all_combine_back",
                       &in_off, &out_off, &nbytes);
   if (rc) return rc;
-  return launch_runs(h, in_off, out_off, W, Sp, (size_t)H * D * elem_bytes, true,
+  return launch_runs(h, in_off, out_off, W, Sp, (size_t)H * D * elem_bytes, true, false,
                      as_stream(stream), "all2all_combine_back");
 }
 

@@ -83,12 +83,19 @@ __device__ __forceinline__ bool cmp_holds(int64_t cur, int cmp, int64_t v) {
   return cmp == kCmpEq ? cur == v : (cmp == kCmpGt ? cur > v : cur < v);
 }
 
-__device__ __forceinline__ void record_timeout(Control* ctl, const void* heap_base,
-                                               const int64_t* sig) {
-  if (atomicCAS(reinterpret_cast<int*>(&ctl->error), 0, kErrTimedOut) == 0)
-    ctl->error_info = (int64_t)((const char*)sig - (const char*)heap_base);
+__device__ __forceinline__ void record_error(Control* ctl, int code, int64_t info) {
+  if (atomicCAS(reinterpret_cast<int*>(&ctl->error), 0, code) == 0) ctl->error_info = info;
   st_relaxed_u32(&ctl->abort, 1u);
 }
+__device__ __forceinline__ void record_timeout(Control* ctl, const void* heap_base,
+                                               const int64_t* sig) {
+  record_error(ctl, kErrTimedOut, (int64_t)((const char*)sig - (const char*)heap_base));
+}
+
+// Longest sleep between two polls of a spin, in ns (0: poll without sleeping).
+#ifndef SYMM_SPIN_MAX_SLEEP_NS
+#define SYMM_SPIN_MAX_SLEEP_NS 256
+#endif
 
 // Spin (one thread) until `*sig cmp v` holds, with acquire semantics.  Gives
 // up after `budget_ns` of %globaltimer time, or after an iteration cap that
@@ -96,10 +103,12 @@ __device__ __forceinline__ void record_timeout(Control* ctl, const void* heap_ba
 // has raised the abort flag.  Never traps.
 __device__ __forceinline__ int spin_wait(const int64_t* sig, int cmp, int64_t v, uint64_t budget_ns,
                                          Control* ctl, const void* heap_base) {
+  if (cmp_holds(ld_acquire(sig), cmp, v)) return kSpinOk;
   const uint64_t t0 = globaltimer_ns();
-  // each round sleeps >= 64 ns, so this cap is >= ~budget/2 of wall time
-  const uint64_t max_iters = budget_ns / 128 + 4096;
-  uint32_t backoff = 32;
+  // a poll takes >= ~16 ns, so this cap is >= ~budget/4 of wall time even if
+  // the timer stood still
+  const uint64_t max_iters = budget_ns / 64 + 4096;
+  uint32_t backoff = 16;
   for (uint64_t it = 0;; ++it) {
     if (cmp_holds(ld_acquire(sig), cmp, v)) return kSpinOk;
     if (ld_relaxed_u32(&ctl->abort)) return kSpinAborted;
@@ -107,8 +116,10 @@ __device__ __forceinline__ int spin_wait(const int64_t* sig, int cmp, int64_t v,
       record_timeout(ctl, heap_base, sig);
       return kSpinTimeout;
     }
-    __nanosleep(backoff);
-    if (backoff < 256) backoff <<= 1;
+    if (SYMM_SPIN_MAX_SLEEP_NS > 0) {
+      __nanosleep(backoff);
+      if (backoff < SYMM_SPIN_MAX_SLEEP_NS) backoff <<= 1;
+    }
   }
 }
 
@@ -261,6 +272,83 @@ __device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, size
   }
   const size_t done = head + (nvec << 4);
   if ((size_t)lane < n - done) st1(dst + done + lane, ld1<LK>(src + done + lane));
+}
+
+// ------------------------------------------------ bulk (TMA) copies -------
+// Bulk copies run in the async proxy: a global->shared copy completes on an
+// mbarrier (complete_tx), a shared->global copy in a bulk group.  Both need
+// 16-byte-aligned addresses and a size that is a multiple of 16.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+// Makes mbarrier initialisation visible to the async proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with `parity` of an mbarrier, at most budget_ns (or
+// an iteration cap if the timer stood still).  Returns false on give-up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  const uint64_t max_iters = budget_ns / 64 + (1u << 20);
+  for (uint64_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > budget_ns || it > max_iters) return false;
+  }
+}
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// All but the newest N bulk groups have finished reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// All but the newest N bulk groups have completed their global writes.
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Orders generic-proxy accesses to this CTA's shared memory before later
+// async-proxy (bulk copy) accesses to it, and vice versa.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Orders generic-proxy and async-proxy accesses to global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 }  // namespace symm

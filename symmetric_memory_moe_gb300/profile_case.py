@@ -1,0 +1,92 @@
+"""Runs one all-to-all variant on one shape for a few steps (for profilers
+such as ncu, or quick timing), through the C ABI.
+
+  python -m symmetric_memory_moe_gb300.profile_case --variant pc --S 256 --steps 4
+
+Each step is the whole call (for pc: the signal reset and the pipeline).
+Prints one JSON line with per-step CUDA-event times and GB/s (2 x input
+bytes / time).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import statistics
+
+import torch
+
+from . import abi
+from .torch_heap import CombineBuffers
+
+DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "int32": torch.int32,
+          "uint8": torch.uint8}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--variant", default="pc",
+                    choices=["direct", "pc", "noalloc", "dispatch", "combine_back"])
+    ap.add_argument("--W", type=int, default=8)
+    ap.add_argument("--S", type=int, default=256)
+    ap.add_argument("--H", type=int, default=1)
+    ap.add_argument("--D", type=int, default=7168)
+    ap.add_argument("--dtype", default="bf16", choices=sorted(DTYPES))
+    ap.add_argument("--tile-s", type=int, default=16)
+    ap.add_argument("--block-d", type=int, default=1024)
+    ap.add_argument("--buffers", type=int, default=2)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--vector", action="store_true",
+                    help="force 16-byte vector copies instead of bulk (TMA) copies")
+    args = ap.parse_args(argv)
+
+    dt = DTYPES[args.dtype]
+    es = torch.empty((), dtype=dt).element_size()
+    W, S, H, D = args.W, args.S, args.H, args.D
+    rows_in = S * W if args.variant in ("direct", "pc", "noalloc") else S
+    if args.variant == "combine_back":
+        rows_in = S  # per PE (S/W, H*W, D): same bytes as (S, H, D)
+    bufs = CombineBuffers(W, rows_in, H, D, es, pc=args.variant == "pc", S=S,
+                          tile_s=args.tile_s, block_d=args.block_d, buffer_num=args.buffers)
+    heap = bufs.heap
+    # the path moves raw bits, so seeded random bytes drawn on the device
+    # stand in for the workload's values here
+    g = torch.Generator(device=heap.mem.device).manual_seed(7)
+    heap.views(bufs.inp, bufs.nbytes).copy_(
+        torch.randint(0, 256, (W, bufs.nbytes), generator=g, dtype=torch.uint8,
+                      device=heap.mem.device))
+
+    def step():
+        if args.variant in ("direct", "pc"):
+            kind = abi.SYMM_A2A_PC if args.variant == "pc" else abi.SYMM_A2A_DIRECT
+            if args.vector:
+                kind |= abi.SYMM_A2A_FLAG_VECTOR
+            abi.all2all_combine(heap.handle, bufs.inp, bufs.out, W, S, H, D, es, kind,
+                                args.tile_s, args.block_d, args.buffers, bufs.staging,
+                                bufs.signals)
+        elif args.variant == "noalloc":
+            abi.all2all_combine_pc_noalloc(heap.handle, bufs.inp, bufs.out, W, S, H, D, es,
+                                           args.tile_s, args.block_d, args.buffers)
+        elif args.variant == "dispatch":
+            abi.all2all_dispatch(heap.handle, bufs.inp, bufs.out, W, S, H, D, es)
+        else:
+            abi.all2all_combine_back(heap.handle, bufs.inp, bufs.out, W, S // W, H, D, es)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record()
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    rc, info = abi.symm_check_error(heap.handle)
+    if rc != abi.SYMM_OK:
+        raise SystemExit(f"device wait timed out at signal offset {info}")
+    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    moved = 2 * W * bufs.nbytes
+    print(json.dumps({"variant": args.variant, "W": W, "S": S, "H": H, "D": D, "es": es,
+                      "bytes_per_step": moved, "ms": [round(m, 4) for m in ms],
+                      "gbs_median": round(moved / (statistics.median(ms) * 1e-3) / 1e9, 1)}))
+    heap.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -40,11 +40,18 @@ def _np_view(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
+# variant name -> all2all_combine variant bits: the default picks bulk (TMA)
+# copies for 16-byte-aligned rows; "_vec" forces the 16-byte vector path
+KINDS = {"direct": abi.SYMM_A2A_DIRECT, "pc": abi.SYMM_A2A_PC,
+         "direct_vec": abi.SYMM_A2A_DIRECT | abi.SYMM_A2A_FLAG_VECTOR,
+         "pc_vec": abi.SYMM_A2A_PC | abi.SYMM_A2A_FLAG_VECTOR}
+
+
 def run_combine(x: torch.Tensor, W, S, H, D, variant, tile_s=16, block_d=0, buffer_num=2,
                 in_shift=0, out_shift=0, repeat=1):
     """Runs all2all_combine on x ([W][S*W][H][D], CPU); returns [W, bytes] uint8."""
     es = x.element_size()
-    pc = variant == "pc"
+    pc = variant.startswith("pc")
     extra = 2048
     bufs = CombineBuffers(W, S * W, H, D, es, pc=pc, S=S, tile_s=tile_s, block_d=block_d,
                           buffer_num=buffer_num, extra=extra)
@@ -52,7 +59,7 @@ def run_combine(x: torch.Tensor, W, S, H, D, variant, tile_s=16, block_d=0, buff
     inp, out = bufs.inp + in_shift, bufs.out + out_shift
     heap.upload(inp, x.reshape(W, -1))
     heap.views(out, n).fill_(POISON)
-    kind = abi.SYMM_A2A_PC if pc else abi.SYMM_A2A_DIRECT
+    kind = KINDS[variant]
     for _ in range(repeat):
         abi.all2all_combine(heap.handle, inp, out, W, S, H, D, es, kind, tile_s, block_d,
                             buffer_num, bufs.staging, bufs.signals)
@@ -83,7 +90,8 @@ def assert_bits_equal(got: torch.Tensor, want: np.ndarray):
 # ------------------------------------------------ the five workloads ------
 @pytest.mark.parametrize("name,variant", [
     ("tiny", "direct"), ("tiny", "pc"), ("small", "direct"), ("small", "pc"),
-    ("tail", "direct"), ("tail", "pc"), ("dsv3", "direct"), ("dsv3", "pc")])
+    ("small", "direct_vec"), ("small", "pc_vec"), ("tail", "direct"), ("tail", "pc"),
+    ("dsv3", "direct"), ("dsv3", "pc"), ("dsv3", "direct_vec"), ("dsv3", "pc_vec")])
 def test_workload_combine_bit_exact(name, variant):
     wl, x = _workload_data(name)
     got = run_combine(x, wl.W, wl.S, wl.H, wl.D, variant, tile_s=wl.tile_s,
@@ -135,8 +143,11 @@ def _rand_bytes(W, rows, H, D, es, seed):
     (2, 5, 4, 16, 8, 2, 5, 2),        # 8-byte elements
     (8, 12, 1, 1, 16, 5, 0, 2),       # 16-byte elements, one element per run
     (6, 3, 3, 100, 4, 64, 17, 2),     # tile taller than S
+    (4, 21, 2, 24, 2, 8, 16, 2),      # 16-byte rows: bulk path, ragged S and D blocks
+    (3, 10, 1, 40000, 2, 2, 0, 2),    # 80 kB runs: several bulk chunks per run
+    (2, 33, 4, 8, 4, 4, 4, 3),        # 16-byte rows of 4-byte elements, 3 buffers
 ])
-@pytest.mark.parametrize("variant", ["direct", "pc"])
+@pytest.mark.parametrize("variant", ["direct", "pc", "direct_vec", "pc_vec"])
 def test_shapes(W, S, H, D, es, tile_s, block_d, buf, variant):
     xe = _rand_bytes(W, S * W, H, D, es, seed=W * 1000 + S).reshape(W, S * W, H, D, es)
     got = _run_es(xe, W, S, H, D, es, variant, tile_s, block_d, buf)
@@ -150,16 +161,15 @@ def _expect_es(xe, W, S, H, D, es):
 
 
 def _run_es(xe, W, S, H, D, es, variant, tile_s, block_d, buf, in_shift=0, out_shift=0):
-    pc = variant == "pc"
+    pc = variant.startswith("pc")
     bufs = CombineBuffers(W, S * W, H, D, es, pc=pc, S=S, tile_s=tile_s, block_d=block_d,
                           buffer_num=buf, extra=2048)
     heap, n = bufs.heap, bufs.nbytes
     inp, out = bufs.inp + in_shift, bufs.out + out_shift
     heap.upload(inp, xe.reshape(W, -1))
     heap.views(out, n).fill_(POISON)
-    kind = abi.SYMM_A2A_PC if pc else abi.SYMM_A2A_DIRECT
-    abi.all2all_combine(heap.handle, inp, out, W, S, H, D, es, kind, tile_s, block_d, buf,
-                        bufs.staging, bufs.signals)
+    abi.all2all_combine(heap.handle, inp, out, W, S, H, D, es, KINDS[variant], tile_s, block_d,
+                        buf, bufs.staging, bufs.signals)
     torch.cuda.synchronize()
     assert abi.symm_check_error(heap.handle)[0] == abi.SYMM_OK
     res = heap.download(out, n)
