@@ -57,10 +57,15 @@ extern "C" {
 /* OR-ed into the variant: skip the signal reset that precedes a PC launch
  * (the caller has zeroed the signal slots itself) */
 #define SYMM_A2A_FLAG_NO_RESET 0x100
-/* OR-ed into the variant: move data with 16-byte vector loads/stores even
- * where bulk (TMA) copies through shared memory apply.  By default a launch
- * whose rows are all 16-byte aligned uses bulk copies. */
+/* Copy paths.  By default each variant uses the path measured fastest on
+ * GB300: DIRECT moves 16-byte vectors through registers; PC prefetches the
+ * producer's input tiles with bulk (TMA) copies into shared memory when
+ * every tile row is 16-byte aligned (16-byte vectors otherwise).
+ * OR-ed into the variant: SYMM_A2A_FLAG_VECTOR makes PC use 16-byte vectors
+ * only; SYMM_A2A_FLAG_BULK makes DIRECT use bulk (TMA) copies through
+ * shared memory where every run is 16-byte aligned. */
 #define SYMM_A2A_FLAG_VECTOR 0x200
+#define SYMM_A2A_FLAG_BULK 0x400
 
 /* bytes at the start of every slab that the heap keeps for itself */
 #define SYMM_HEAP_HEADER_BYTES 4096

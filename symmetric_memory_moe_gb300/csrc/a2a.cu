@@ -50,7 +50,7 @@ namespace {
 // Tuning knobs (compile-time): 16-byte vectors in flight per lane, and the
 // minimum resident CTAs per SM that register allocation must allow.
 #ifndef SYMM_RUNS_UNROLL
-#define SYMM_RUNS_UNROLL 4
+#define SYMM_RUNS_UNROLL 8
 #endif
 #ifndef SYMM_RUNS_MIN_BLOCKS
 #define SYMM_RUNS_MIN_BLOCKS 1
@@ -420,17 +420,18 @@ int check_perm(symm_heap* h, const void* in, const void* out, int W, size_t rows
   return SYMM_OK;
 }
 
-// Launches the run permutation; bulk (TMA) copies when every run is 16-byte
-// aligned and `vector_only` is false, 16-byte vector loads/stores otherwise.
+// Launches the run permutation with 16-byte vector loads/stores (measured
+// fastest), or bulk (TMA) copies when `bulk` is asked and every run is
+// 16-byte aligned.
 int launch_runs(symm_heap* h, size_t in_off, size_t out_off, uint32_t W, uint32_t Sb, size_t R,
-                bool inverse, bool vector_only, cudaStream_t s, const char* what) {
+                bool inverse, bool bulk_asked, cudaStream_t s, const char* what) {
   const size_t nruns = (size_t)W * W * Sb;
   if (nruns == 0 || R == 0) return SYMM_OK;
   if (nruns > 0x7fffffffull)
     return fail(SYMM_EINVAL, std::string(what) + ": more than 2^31 runs");
   const uint8_t* in = h->base + in_off;
   uint8_t* out = h->base + out_off;
-  const bool bulk = !vector_only && R % 16 == 0 && in_off % 16 == 0 && out_off % 16 == 0;
+  const bool bulk = bulk_asked && R % 16 == 0 && in_off % 16 == 0 && out_off % 16 == 0;
   if (bulk) {
     int rc = ensure_ctrl(h, s);
     if (rc) return rc;
@@ -570,12 +571,12 @@ extern "C" int all2all_combine(symm_heap_t* h, const void* in, void* out, int W,
                       &out_off, &nbytes);
   if (rc) return rc;
   const int kind = variant & 0xff, flags = variant & ~0xff;
-  if (flags & ~(SYMM_A2A_FLAG_NO_RESET | SYMM_A2A_FLAG_VECTOR))
+  if (flags & ~(SYMM_A2A_FLAG_NO_RESET | SYMM_A2A_FLAG_VECTOR | SYMM_A2A_FLAG_BULK))
     return fail(SYMM_EINVAL, "all2all_combine: unknown flag");
   cudaStream_t s = as_stream(stream);
   if (kind == SYMM_A2A_DIRECT)
     return launch_runs(h, in_off, out_off, W, S, (size_t)H * D * elem_bytes, false,
-                       (flags & SYMM_A2A_FLAG_VECTOR) != 0, s, "all2all_combine");
+                       (flags & SYMM_A2A_FLAG_BULK) != 0, s, "all2all_combine");
   if (kind == SYMM_A2A_PC)
     return combine_pc(h, in_off, out_off, nbytes, W, S, H, D, elem_bytes, flags, tile_s, block_d,
                       buffer_num, staging, signals, s);

@@ -36,7 +36,9 @@ def main(argv=None):
     ap.add_argument("--buffers", type=int, default=2)
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--vector", action="store_true",
-                    help="force 16-byte vector copies instead of bulk (TMA) copies")
+                    help="pc: 16-byte vector copies only (no bulk prefetch)")
+    ap.add_argument("--bulk", action="store_true",
+                    help="direct: bulk (TMA) copies through shared memory")
     args = ap.parse_args(argv)
 
     dt = DTYPES[args.dtype]
@@ -60,6 +62,8 @@ def main(argv=None):
             kind = abi.SYMM_A2A_PC if args.variant == "pc" else abi.SYMM_A2A_DIRECT
             if args.vector:
                 kind |= abi.SYMM_A2A_FLAG_VECTOR
+            if args.bulk:
+                kind |= abi.SYMM_A2A_FLAG_BULK
             abi.all2all_combine(heap.handle, bufs.inp, bufs.out, W, S, H, D, es, kind,
                                 args.tile_s, args.block_d, args.buffers, bufs.staging,
                                 bufs.signals)

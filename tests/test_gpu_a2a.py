@@ -40,10 +40,12 @@ def _np_view(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
-# variant name -> all2all_combine variant bits: the default picks bulk (TMA)
-# copies for 16-byte-aligned rows; "_vec" forces the 16-byte vector path
+# variant name -> all2all_combine variant bits: "direct" copies 16-byte
+# vectors, "direct_bulk" bulk (TMA) copies where rows are 16-byte aligned;
+# "pc" prefetches the producer's input by bulk copies where rows are 16-byte
+# aligned, "pc_vec" uses 16-byte vectors only
 KINDS = {"direct": abi.SYMM_A2A_DIRECT, "pc": abi.SYMM_A2A_PC,
-         "direct_vec": abi.SYMM_A2A_DIRECT | abi.SYMM_A2A_FLAG_VECTOR,
+         "direct_bulk": abi.SYMM_A2A_DIRECT | abi.SYMM_A2A_FLAG_BULK,
          "pc_vec": abi.SYMM_A2A_PC | abi.SYMM_A2A_FLAG_VECTOR}
 
 
@@ -90,8 +92,8 @@ def assert_bits_equal(got: torch.Tensor, want: np.ndarray):
 # ------------------------------------------------ the five workloads ------
 @pytest.mark.parametrize("name,variant", [
     ("tiny", "direct"), ("tiny", "pc"), ("small", "direct"), ("small", "pc"),
-    ("small", "direct_vec"), ("small", "pc_vec"), ("tail", "direct"), ("tail", "pc"),
-    ("dsv3", "direct"), ("dsv3", "pc"), ("dsv3", "direct_vec"), ("dsv3", "pc_vec")])
+    ("small", "direct_bulk"), ("small", "pc_vec"), ("tail", "direct"), ("tail", "pc"),
+    ("dsv3", "direct"), ("dsv3", "pc"), ("dsv3", "direct_bulk"), ("dsv3", "pc_vec")])
 def test_workload_combine_bit_exact(name, variant):
     wl, x = _workload_data(name)
     got = run_combine(x, wl.W, wl.S, wl.H, wl.D, variant, tile_s=wl.tile_s,
@@ -146,8 +148,9 @@ def _rand_bytes(W, rows, H, D, es, seed):
     (4, 21, 2, 24, 2, 8, 16, 2),      # 16-byte rows: bulk path, ragged S and D blocks
     (3, 10, 1, 40000, 2, 2, 0, 2),    # 80 kB runs: several bulk chunks per run
     (2, 33, 4, 8, 4, 4, 4, 3),        # 16-byte rows of 4-byte elements, 3 buffers
+    (2, 9, 1, 16, 2, 2, 8, 1),        # aligned, one buffer: each slot reused by the next task
 ])
-@pytest.mark.parametrize("variant", ["direct", "pc", "direct_vec", "pc_vec"])
+@pytest.mark.parametrize("variant", ["direct", "pc", "direct_bulk", "pc_vec"])
 def test_shapes(W, S, H, D, es, tile_s, block_d, buf, variant):
     xe = _rand_bytes(W, S * W, H, D, es, seed=W * 1000 + S).reshape(W, S * W, H, D, es)
     got = _run_es(xe, W, S, H, D, es, variant, tile_s, block_d, buf)
