@@ -59,9 +59,9 @@ def _traffic(kernel: str, launch_bytes: int):
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
-        if t.get("sources_hash") != _kernel_sources_hash():
-            return None
         e = t["kernels"][kernel]
+        if e.get("sources_hash") != _kernel_sources_hash():
+            return None
         # scaled from the captured launch by the bytes one launch moves
         return int(round(e["dram_bytes"] * launch_bytes / e["algorithmic_bytes"]))
     except Exception:

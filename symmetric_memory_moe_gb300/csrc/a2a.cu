@@ -49,11 +49,21 @@ namespace {
 
 // Tuning knobs (compile-time): 16-byte vectors in flight per lane, and the
 // minimum resident CTAs per SM that register allocation must allow.
+// Run copies: layouts whose runs are all 16-byte aligned use the aligned
+// copy with SYMM_RUNS_UNROLL vectors in flight per lane; any other layout
+// uses the general copy (head/tail bytes, shift-merge) with fewer vectors in
+// flight and more resident warps, which measured faster there.
 #ifndef SYMM_RUNS_UNROLL
-#define SYMM_RUNS_UNROLL 8
+#define SYMM_RUNS_UNROLL 16
 #endif
 #ifndef SYMM_RUNS_MIN_BLOCKS
-#define SYMM_RUNS_MIN_BLOCKS 1
+#define SYMM_RUNS_MIN_BLOCKS 2
+#endif
+#ifndef SYMM_RUNS_GENERAL_UNROLL
+#define SYMM_RUNS_GENERAL_UNROLL 2
+#endif
+#ifndef SYMM_RUNS_GENERAL_MIN_BLOCKS
+#define SYMM_RUNS_GENERAL_MIN_BLOCKS 6
 #endif
 #ifndef SYMM_PC_UNROLL
 #define SYMM_PC_UNROLL 4
@@ -74,8 +84,9 @@ constexpr int kPcMinBlocks = SYMM_PC_MIN_BLOCKS;
 // INVERSE = true (combine_back):
 //   run k = (r*W + d)*Sb + s : in slab d row s*W + r   ->  out slab r row d*Sb + s
 // (a "row" here is one run of R bytes).
-template <bool INVERSE>
-__global__ void __launch_bounds__(kRunThreads, SYMM_RUNS_MIN_BLOCKS)
+template <bool INVERSE, bool ALIGNED>
+__global__ void __launch_bounds__(kRunThreads,
+                                  ALIGNED ? SYMM_RUNS_MIN_BLOCKS : SYMM_RUNS_GENERAL_MIN_BLOCKS)
     a2a_runs_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, size_t slab,
                     uint32_t W, uint32_t Sb, size_t R, uint32_t nruns) {
   const int lane = threadIdx.x & 31;
@@ -93,7 +104,11 @@ __global__ void __launch_bounds__(kRunThreads, SYMM_RUNS_MIN_BLOCKS)
       src = in + d * slab + (size_t)(s * W + r) * R;
       dst = out + r * slab + (size_t)(d * Sb + s) * R;
     }
-    symm::warp_copy<SYMM_RUNS_UNROLL, symm::kRO, symm::kCS>(dst, src, R, lane);
+    if (ALIGNED)
+      symm::warp_copy_aligned<SYMM_RUNS_UNROLL, symm::kRO, symm::kCS>(dst, src, R >> 4, lane);
+    else
+      symm::warp_copy<SYMM_RUNS_GENERAL_UNROLL, symm::kRO, symm::kCS, SYMM_RUNS_GENERAL_UNROLL>(
+          dst, src, R, lane);
   }
 }
 
@@ -453,16 +468,24 @@ int launch_runs(symm_heap* h, size_t in_off, size_t out_off, uint32_t W, uint32_
                                                               h->spin_budget, ctl);
     return cuda_check(cudaGetLastError(), what);
   }
-  const void* kfn = inverse ? (const void*)a2a_runs_kernel<true> : (const void*)a2a_runs_kernel<false>;
+  const bool aligned = R % 16 == 0 && in_off % 16 == 0 && out_off % 16 == 0;
+  const void* kfn = inverse ? (aligned ? (const void*)a2a_runs_kernel<true, true>
+                                       : (const void*)a2a_runs_kernel<true, false>)
+                            : (aligned ? (const void*)a2a_runs_kernel<false, true>
+                                       : (const void*)a2a_runs_kernel<false, false>);
   int cap = resident_ctas(kfn, kRunThreads);
   if (cap <= 0) cap = 4 * (sm_count() > 0 ? sm_count() : 1);
   const size_t need = (nruns + kRunThreads / 32 - 1) / (kRunThreads / 32);
   const int grid = (int)(need < (size_t)cap ? need : (size_t)cap);
-  if (inverse)
-    a2a_runs_kernel<true><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R, (uint32_t)nruns);
+  const uint32_t n32 = (uint32_t)nruns;
+  if (inverse && aligned)
+    a2a_runs_kernel<true, true><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R, n32);
+  else if (inverse)
+    a2a_runs_kernel<true, false><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R, n32);
+  else if (aligned)
+    a2a_runs_kernel<false, true><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R, n32);
   else
-    a2a_runs_kernel<false><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R,
-                                                        (uint32_t)nruns);
+    a2a_runs_kernel<false, false><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R, n32);
   return cuda_check(cudaGetLastError(), what);
 }
 

@@ -189,6 +189,27 @@ __device__ __forceinline__ uint8_t ld1(const uint8_t* p) {
   return ld1_cg(p);
 }
 
+// One warp copies nvec 16-byte vectors; src and dst are 16-byte aligned.
+template <int U, int LK, int SK>
+__device__ __forceinline__ void warp_copy_aligned(uint8_t* dst, const uint8_t* src, size_t nvec,
+                                                  int lane) {
+  size_t j = lane;
+  for (; j + 32 * (U - 1) < nvec; j += 32 * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = ld16<LK>(src + 16 * (j + 32 * u));
+#pragma unroll
+    for (int u = 0; u < U; ++u) st16k<SK>(dst + 16 * (j + 32 * u), v[u]);
+  }
+  uint4 v[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (j + 32 * u < nvec) v[u] = ld16<LK>(src + 16 * (j + 32 * u));
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (j + 32 * u < nvec) st16k<SK>(dst + 16 * (j + 32 * u), v[u]);
+}
+
 // Bytes m..m+15 (1 <= m <= 15) of the 32-byte little-endian concatenation a|b.
 __device__ __forceinline__ uint4 funnel16(uint4 a, uint4 b, unsigned m) {
   uint64_t w0 = (uint64_t)a.x | ((uint64_t)a.y << 32);
@@ -218,8 +239,9 @@ __device__ __forceinline__ uint4 funnel16(uint4 a, uint4 b, unsigned m) {
 //    funnel-shifts the pair (a block read past the end of src stays inside
 //    src's 16-byte-aligned, 16-byte-padded allocation);
 //  * tail: the last < 16 bytes, one byte per lane.
-// U = 16-byte vectors in flight per lane.
-template <int U, int LK, int SK>
+// U = 16-byte vectors in flight per lane on the aligned path, V on the
+// shift-merge path (default U/2: each output needs two source blocks).
+template <int U, int LK, int SK, int V = (U > 1 ? U / 2 : 1)>
 __device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, size_t n, int lane) {
   if (n == 0) return;
   size_t head = (16 - ((uintptr_t)dst & 15)) & 15;
@@ -246,9 +268,7 @@ __device__ __forceinline__ void warp_copy(uint8_t* dst, const uint8_t* src, size
     for (int u = 0; u < U; ++u)
       if (j + 32 * u < nvec) st16k<SK>(d + 16 * (j + 32 * u), v[u]);
   } else if (nvec) {
-    // aligned source blocks a[0..nvec] (nvec+1 of them) cover the body;
-    // half the vectors in flight of the aligned path (two blocks per output)
-    constexpr int V = U > 1 ? U / 2 : 1;
+    // aligned source blocks a[0..nvec] (nvec+1 of them) cover the body
     const uint8_t* a0 = s - m;
     for (size_t base = 0; base < nvec; base += 32 * V) {  // warp-uniform loop
       uint4 a[V];
