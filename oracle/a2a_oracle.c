@@ -283,3 +283,62 @@ int oracle_put_with_signal(void *heap, int64_t slab_stride, int64_t npes,
     if (rc) return rc;
     return oracle_signal_op(heap, slab_stride, npes, sig_off, value, op, pe);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Collectives built on the one-sided primitives: HyperParallel RFC          */
+/* "Symmetric Memory", section 10 (advanced algorithms, push mode).          */
+/* ------------------------------------------------------------------------ */
+
+/* AllToAll with per-pair row counts (push mode).  counts[r*W + d] rows of   */
+/* row_bytes go from PE r to PE d.  PE r's input holds its rows for d = 0,   */
+/* 1, ... back to back; PE d's output holds the rows it receives from r = 0, */
+/* 1, ... back to back (the receive offsets the RFC exchanges first).        */
+/*   in  [W][in_rows][row_bytes]    out [W][out_rows][row_bytes]            */
+/* Output rows past what PE d receives are left untouched.  Returns -1 when  */
+/* a count is negative or a PE would send or receive more rows than fit.     */
+int oracle_alltoallv(const void *in, void *out, const int64_t *counts, int64_t W,
+                     int64_t row_bytes, int64_t in_rows, int64_t out_rows)
+{
+    if (W < 1 || row_bytes < 0 || in_rows < 0 || out_rows < 0) return -1;
+    for (int64_t r = 0; r < W; r++) {
+        int64_t sent = 0;
+        for (int64_t d = 0; d < W; d++) {
+            if (counts[r * W + d] < 0) return -1;
+            sent += counts[r * W + d];
+        }
+        if (sent > in_rows) return -1;
+    }
+    for (int64_t d = 0; d < W; d++) {
+        int64_t got = 0;
+        for (int64_t r = 0; r < W; r++) got += counts[r * W + d];
+        if (got > out_rows) return -1;
+    }
+    const unsigned char *src = (const unsigned char *)in;
+    unsigned char *dst = (unsigned char *)out;
+    for (int64_t d = 0; d < W; d++) {
+        int64_t pos = 0;                               /* next receive row of d */
+        for (int64_t r = 0; r < W; r++) {
+            int64_t first = 0;                         /* r's first row for d */
+            for (int64_t e = 0; e < d; e++) first += counts[r * W + e];
+            for (int64_t i = 0; i < counts[r * W + d]; i++) {
+                memcpy(dst + (d * out_rows + pos) * row_bytes,
+                       src + (r * in_rows + first + i) * row_bytes, (size_t)row_bytes);
+                pos++;
+            }
+        }
+    }
+    return 0;
+}
+
+/* AllGather (push mode): every PE r places its `bytes` at byte r*bytes of  */
+/* every PE's output.   in [W][bytes]   out [W][W*bytes]                     */
+int oracle_allgather(const void *in, void *out, int64_t W, int64_t bytes)
+{
+    if (W < 1 || bytes < 0) return -1;
+    const unsigned char *src = (const unsigned char *)in;
+    unsigned char *dst = (unsigned char *)out;
+    for (int64_t d = 0; d < W; d++)
+        for (int64_t r = 0; r < W; r++)
+            memcpy(dst + (d * W + r) * bytes, src + r * bytes, (size_t)bytes);
+    return 0;
+}

@@ -62,6 +62,10 @@ class Oracle:
         for name in ("oracle_put", "oracle_get", "oracle_signal_op", "oracle_wait_satisfied",
                      "oracle_put_with_signal"):
             getattr(lib, name).restype = ctypes.c_int
+        lib.oracle_alltoallv.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64]
+        lib.oracle_alltoallv.restype = ctypes.c_int
+        lib.oracle_allgather.argtypes = [_P, _P, _I64, _I64]
+        lib.oracle_allgather.restype = ctypes.c_int
         self.lib = lib
 
     # -- permutations ------------------------------------------------------
@@ -118,6 +122,35 @@ class Oracle:
         if rc:
             raise ValueError(f"oracle_pc_replay rc={rc}")
         return out, signals
+
+    def alltoallv(self, x: np.ndarray, counts: np.ndarray, out_rows: int,
+                  out: np.ndarray | None = None) -> np.ndarray:
+        """x: [W, in_rows, ...] rows; counts: [W, W] int64, counts[r, d] rows
+        from r to d -> out [W, out_rows, ...] (rows not received keep `out`'s
+        values, zeros when out is None)."""
+        x = np.ascontiguousarray(x)
+        W, in_rows = x.shape[0], x.shape[1]
+        row_bytes = x[0, 0].nbytes if in_rows else int(np.prod(x.shape[2:])) * x.itemsize
+        c = np.ascontiguousarray(counts, dtype=np.int64)
+        assert c.shape == (W, W)
+        if out is None:
+            out = np.zeros((W, out_rows) + x.shape[2:], dtype=x.dtype)
+        out = np.ascontiguousarray(out)
+        rc = self.lib.oracle_alltoallv(self._ptr(x), self._ptr(out), self._ptr(c), W, row_bytes,
+                                       in_rows, out_rows)
+        if rc:
+            raise ValueError(f"oracle_alltoallv rc={rc}")
+        return out
+
+    def allgather(self, x: np.ndarray) -> np.ndarray:
+        """x: [W, n] -> [W, W*n]."""
+        x = np.ascontiguousarray(x)
+        W = x.shape[0]
+        out = np.empty((W, W * x[0].size), dtype=x.dtype)
+        rc = self.lib.oracle_allgather(self._ptr(x), self._ptr(out), W, x[0].nbytes)
+        if rc:
+            raise ValueError(f"oracle_allgather rc={rc}")
+        return out
 
     # -- primitives on a host-memory heap -----------------------------------
     def put(self, heap: np.ndarray, slab: int, npes: int, target_off: int, src: np.ndarray,

@@ -200,6 +200,88 @@ def pin_primitives(o):
     assert o.signal_op(heap, slab, W, 192, 1, 2, 0) != 0    # no op 2
 
 
+# -- collectives: AllToAll with uneven counts, AllGather ---------------------
+GOLDEN_A2AV = os.path.join(HERE, "golden", "alltoallv_w2.txt")
+
+
+def _random_counts(W, seed, hi=5, zero_frac=0.3):
+    rng = np.random.default_rng(seed)
+    c = rng.integers(0, hi, size=(W, W)).astype(np.int64)
+    c[rng.random((W, W)) < zero_frac] = 0
+    return c
+
+
+def pin_alltoallv_golden(o):
+    """Hand-worked W=2 uneven exchange (rows are one int32)."""
+    vals = {}
+    with open(GOLDEN_A2AV) as f:
+        for line in f:
+            line = line.split("#")[0].split()
+            if line:
+                vals.setdefault(line[0], []).append([int(v) for v in line[1:]])
+    counts = np.array(vals["counts"][0], np.int64).reshape(2, 2)
+    x = np.array([row[1:] for row in sorted(vals["in"])], np.int32).reshape(2, 3, 1)
+    want = np.array([row[1:] for row in sorted(vals["out"])], np.int32).reshape(2, 4, 1)
+    got = o.alltoallv(x, counts, 4, out=np.full((2, 4, 1), -1, np.int32))
+    np.testing.assert_array_equal(got, want)
+
+
+def pin_alltoallv_w1_and_equal_split(o):
+    """One PE keeps its first n rows; equal counts S are the block transpose
+    of the [r][d][S] view (numpy)."""
+    x = _rand((1, 9, 5), 21, np.int16)
+    np.testing.assert_array_equal(o.alltoallv(x, np.array([[6]]), 9)[0, :6], x[0, :6])
+    for W, S, rb in [(2, 3, 4), (4, 5, 7), (8, 2, 16)]:
+        x = _rand((W, W * S, rb), 22, np.uint8)
+        y = o.alltoallv(x, np.full((W, W), S, np.int64), W * S)
+        ref = x.reshape(W, W, S, rb).transpose(1, 0, 2, 3).reshape(W, W * S, rb)
+        np.testing.assert_array_equal(y, ref)
+
+
+def pin_alltoallv_round_trip_and_bijection(o):
+    """Counts C then C^T bring every sent row home; with iota rows the rows
+    received are exactly the rows sent."""
+    for W, seed in [(2, 1), (5, 2), (8, 3), (3, 4)]:
+        c = _random_counts(W, seed)
+        in_rows = int(c.sum(1).max()) + 2
+        mid_rows = int(c.sum(0).max()) + 1
+        x = np.arange(W * in_rows * 3, dtype=np.int64).reshape(W, in_rows, 3) + 10**6
+        y = o.alltoallv(x, c, mid_rows)
+        back = o.alltoallv(y, c.T.copy(), in_rows)
+        for r in range(W):
+            n = int(c[r].sum())
+            np.testing.assert_array_equal(back[r, :n], x[r, :n])
+        sent = np.concatenate([x[r, :int(c[r].sum())] for r in range(W)]).reshape(-1, 3)
+        got = np.concatenate([y[d, :int(c[:, d].sum())] for d in range(W)]).reshape(-1, 3)
+        assert np.array_equal(np.sort(sent[:, 0]), np.sort(got[:, 0]))
+
+
+def pin_alltoallv_rejects(o):
+    """Negative counts and rows that do not fit are refused."""
+    x = np.zeros((2, 3, 1), np.int32)
+    for c, out_rows in [(np.array([[1, -1], [0, 0]]), 4), (np.array([[2, 2], [0, 0]]), 4),
+                        (np.array([[2, 0], [3, 0]]), 4)]:
+        try:
+            o.alltoallv(x, c, out_rows)
+        except ValueError:
+            continue
+        raise AssertionError(f"accepted counts {c.tolist()}")
+
+
+def pin_allgather(o):
+    """Every PE's output is the concatenation of all inputs in rank order;
+    one PE is the identity."""
+    x = _rand((1, 11), 31, np.uint8)
+    np.testing.assert_array_equal(o.allgather(x), x)
+    for W, n in [(2, 3), (4, 17), (8, 64)]:
+        x = _rand((W, n), 32, np.int16)
+        y = o.allgather(x)
+        for d in range(W):
+            np.testing.assert_array_equal(y[d], x.reshape(-1))
+    x = np.array([[7, 8], [9, 10], [11, 12]], np.int32)
+    assert o.allgather(x)[1].tolist() == [7, 8, 9, 10, 11, 12]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

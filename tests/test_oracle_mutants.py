@@ -39,6 +39,13 @@ MUTANTS = [
     ("oracle_signal_op", "(uint64_t)cur + (uint64_t)value", "(uint64_t)value", "ADD acts as SET"),
     ("oracle_wait_satisfied", "current > value", "current >= value", "GT as GE"),
     ("oracle_wait_satisfied", "current < value", "current > value", "LT as GT"),
+    ("oracle_alltoallv", "first += counts[r * W + e];", "first += counts[e * W + d];",
+     "transposed send offset"),
+    ("oracle_alltoallv", "(d * out_rows + pos) * row_bytes", "(d * out_rows + i) * row_bytes",
+     "receive offset dropped"),
+    ("oracle_alltoallv", "for (int64_t e = 0; e < d; e++)", "for (int64_t e = 0; e <= d; e++)",
+     "off-by-one send offset"),
+    ("oracle_allgather", "(d * W + r) * bytes", "(r * W + d) * bytes", "transposed gather"),
 ]
 
 
