@@ -42,12 +42,14 @@ def _hbm_peak():
         return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
 
 
-def _kernel_sources_hash() -> str:
+def _kernel_sources_hash(files) -> str:
+    """Hash of the csrc files a kernel is compiled from (its translation unit
+    and the headers it includes)."""
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "symmetric_memory_moe_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -60,7 +62,7 @@ def _traffic(kernel: str, launch_bytes: int):
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
         e = t["kernels"][kernel]
-        if e.get("sources_hash") != _kernel_sources_hash():
+        if e.get("sources_hash") != _kernel_sources_hash(e["sources"]):
             return None
         # scaled from the captured launch by the bytes one launch moves
         return int(round(e["dram_bytes"] * launch_bytes / e["algorithmic_bytes"]))

@@ -42,6 +42,7 @@ extern "C" {
 #define SYMM_ENOMEM (-2)    /* the heap's slab has no room for the request */
 #define SYMM_ETIMEDOUT (-3) /* a device-side wait ran past its budget */
 #define SYMM_ECUDA (-4)     /* a CUDA runtime call failed (message in symm_last_error) */
+#define SYMM_ERANGE (-5)    /* device-side sizes (counts) exceed a buffer; reported by symm_check_error */
 
 /* signal operations and comparisons, numbered as the [RFC] Python API numbers
  * them (section 4: signal_op 0=SET, 1=ADD; compare_op 0=EQ, 1=GT, 2=LT) */
@@ -225,6 +226,43 @@ int all2all_combine_host(symm_heap_t *heap, const void *host_in, void *host_out,
                          void *out, int W, int S, int H, int D, int elem_bytes, int variant,
                          int tile_s, int block_d, int buffer_num, void *staging, int64_t *signals,
                          void *stream);
+
+/* --------------------------------------------------------- collectives -- */
+
+/* Bytes of device workspace (plain device memory, 8-byte aligned; no need to
+ * be symmetric) that shmem_alltoall and shmem_allgather need for W PEs:
+ * offsets, per-segment completion counters and a validity word.
+ * Errors: SYMM_EINVAL (W outside [1, 4096]). */
+int shmem_collective_workspace(int W, size_t *bytes);
+
+/* [RFC] 10 (AllToAll, push mode): every PE r sends counts[r*W + d] rows of
+ * row_bytes to every PE d.  PE r's input (symmetric, in_rows rows) holds its
+ * rows for d = 0, 1, ... back to back; PE d's output (symmetric, out_rows
+ * rows) receives the rows of r = 0, 1, ... back to back; output rows past
+ * what PE d receives are not written.
+ * counts      device; W*W int64, read by the kernels (the host never
+ *             synchronises to learn them).  A negative count, a PE sending
+ *             more than in_rows or receiving more than out_rows rows is
+ *             found on the device: nothing is copied and symm_check_error()
+ *             reports SYMM_ERANGE.
+ * workspace   device; shmem_collective_workspace(W) bytes.
+ * signals     symmetric int64 (one per PE): zeroed, then ADDed to (release)
+ *             once per completed (r, d) segment; the call ends with every
+ *             PE's wait for the value W, so on return (in stream order) the
+ *             output is complete.
+ * Errors: SYMM_EINVAL, SYMM_ECUDA; later SYMM_ERANGE/SYMM_ETIMEDOUT via
+ * symm_check_error(). */
+int shmem_alltoall(symm_heap_t *heap, const void *in, void *out, const int64_t *counts, int W,
+                   size_t row_bytes, size_t in_rows, size_t out_rows, void *workspace,
+                   int64_t *signals, void *stream);
+
+/* [RFC] 10 (AllGather, push mode): every PE r pushes its `bytes` (symmetric
+ * `in`) to byte r*bytes of every PE's symmetric `out` (W*bytes per PE) and
+ * ADDs 1 to that PE's signal; the call ends with every PE waiting for W.
+ * workspace and signals as for shmem_alltoall.  Any alignment.
+ * Errors: SYMM_EINVAL, SYMM_ECUDA; later SYMM_ETIMEDOUT via symm_check_error(). */
+int shmem_allgather(symm_heap_t *heap, const void *in, void *out, int W, size_t bytes,
+                    void *workspace, int64_t *signals, void *stream);
 
 /* ------------------------------------------- allocation-free variant -- */
 

@@ -19,6 +19,7 @@ SYMM_EINVAL = -1
 SYMM_ENOMEM = -2
 SYMM_ETIMEDOUT = -3
 SYMM_ECUDA = -4
+SYMM_ERANGE = -5
 SYMM_SIGNAL_SET = 0
 SYMM_SIGNAL_ADD = 1
 SYMM_CMP_EQ = 0
@@ -34,7 +35,7 @@ SYMM_SIGNAL_STRIDE_BYTES = 64
 SYMM_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _NAMES = {SYMM_EINVAL: "SYMM_EINVAL", SYMM_ENOMEM: "SYMM_ENOMEM",
-          SYMM_ETIMEDOUT: "SYMM_ETIMEDOUT", SYMM_ECUDA: "SYMM_ECUDA"}
+          SYMM_ETIMEDOUT: "SYMM_ETIMEDOUT", SYMM_ECUDA: "SYMM_ECUDA", SYMM_ERANGE: "SYMM_ERANGE"}
 
 
 class SymmError(RuntimeError):
@@ -70,6 +71,9 @@ _SIGS = {
     "all2all_combine_back": [_P, _P, _P, _I, _I, _I, _I, _I, _P],
     "all2all_combine_host": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P],
     "all2all_combine_pc_noalloc": [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
+    "shmem_collective_workspace": [_I, ctypes.POINTER(_SZ)],
+    "shmem_alltoall": [_P, _P, _P, _P, _I, _SZ, _SZ, _SZ, _P, _P, _P],
+    "shmem_allgather": [_P, _P, _P, _I, _SZ, _P, _P, _P],
 }
 
 _lock = threading.Lock()
@@ -154,11 +158,12 @@ def symm_set_spin_budget(heap: int, budget_ns: int) -> None:
 
 
 def symm_check_error(heap: int, stream=None):
-    """(code, info): SYMM_OK or SYMM_ETIMEDOUT plus the timed-out signal's byte
-    offset; raises SymmError only for a failure of the check itself."""
+    """(code, info): SYMM_OK, SYMM_ETIMEDOUT (info: the timed-out signal's byte
+    offset) or SYMM_ERANGE; raises SymmError only for a failure of the check
+    itself."""
     info = _I64(0)
     rc = lib().symm_check_error(heap, _stream(stream), ctypes.byref(info))
-    if rc not in (SYMM_OK, SYMM_ETIMEDOUT):
+    if rc not in (SYMM_OK, SYMM_ETIMEDOUT, SYMM_ERANGE):
         _check(rc, "symm_check_error")
     return rc, info.value
 
@@ -234,3 +239,21 @@ def all2all_combine_pc_noalloc(heap, inp, out, W, S, H, D, elem_bytes, tile_s=16
     _check(lib().all2all_combine_pc_noalloc(heap, inp, out, W, S, H, D, elem_bytes, tile_s,
                                             block_d, buffer_num, _stream(stream)),
            "all2all_combine_pc_noalloc")
+
+
+# ------------------------------------------------------------ collectives --
+def shmem_collective_workspace(W: int) -> int:
+    n = _SZ(0)
+    _check(lib().shmem_collective_workspace(W, ctypes.byref(n)), "shmem_collective_workspace")
+    return n.value
+
+
+def shmem_alltoall(heap, inp, out, counts, W, row_bytes, in_rows, out_rows, workspace, signals,
+                   stream=None):
+    _check(lib().shmem_alltoall(heap, inp, out, counts, W, row_bytes, in_rows, out_rows, workspace,
+                                signals, _stream(stream)), "shmem_alltoall")
+
+
+def shmem_allgather(heap, inp, out, W, nbytes, workspace, signals, stream=None):
+    _check(lib().shmem_allgather(heap, inp, out, W, nbytes, workspace, signals, _stream(stream)),
+           "shmem_allgather")

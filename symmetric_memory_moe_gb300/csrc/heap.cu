@@ -252,6 +252,8 @@ extern "C" int symm_check_error(symm_heap_t* h, void* stream, int64_t* info) {
   if (rc) return rc;
   if (info) *info = ctl.error_info;
   const int code = ctl.error ? ctl.error : SYMM_ETIMEDOUT;
+  if (code == SYMM_ERANGE)
+    return fail(code, "device-side sizes exceed a buffer (nothing was copied)");
   return fail(code, "device wait gave up (signal at heap byte offset " +
                         std::to_string(ctl.error_info) + ")");
 }

@@ -105,3 +105,41 @@ def random_bytes(nbytes: int, seed: int) -> torch.Tensor:
     g = torch.Generator("cpu")
     g.manual_seed(seed)
     return torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8)
+
+
+def moe_counts(W: int, tokens: int, experts: int, topk: int, seed: int,
+               skew: float = 1.0) -> torch.Tensor:
+    """Rows each PE sends to each PE under synthetic top-k MoE routing.
+
+    Each of the ``tokens`` tokens on PE r picks ``topk`` distinct experts
+    (``torch.multinomial`` without replacement) from ``experts`` experts whose
+    popularity follows a Zipf law of exponent ``skew`` over a seeded random
+    order; expert e lives on PE ``e // (experts // W)``.  A token travels once
+    to every PE that hosts at least one of its experts, so ``counts[r, d]`` is
+    the number of tokens of PE r with an expert on PE d.  Returns [W, W] int64.
+    """
+    assert experts % W == 0 and 0 < topk <= experts
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    order = torch.randperm(experts, generator=g)
+    weight = torch.empty(experts, dtype=torch.float64)
+    weight[order] = 1.0 / torch.arange(1, experts + 1, dtype=torch.float64) ** skew
+    counts = torch.zeros(W, W, dtype=torch.int64)
+    per_pe = experts // W
+    for r in range(W):
+        picked = torch.multinomial(weight.expand(tokens, experts), topk, replacement=False,
+                                   generator=g)
+        hit = torch.zeros(tokens, W, dtype=torch.bool)
+        hit.scatter_(1, picked // per_pe, True)
+        counts[r] = hit.sum(0)
+    return counts
+
+
+def random_counts(W: int, high: int, seed: int, zero_frac: float = 0.0) -> torch.Tensor:
+    """[W, W] int64 counts uniform in [0, high), a ``zero_frac`` share set to 0."""
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    c = torch.randint(0, high, (W, W), generator=g, dtype=torch.int64)
+    if zero_frac > 0:
+        c[torch.rand(W, W, generator=g) < zero_frac] = 0
+    return c

@@ -3,9 +3,12 @@ such as ncu, or quick timing), through the C ABI.
 
   python -m symmetric_memory_moe_gb300.profile_case --variant pc --S 256 --steps 4
 
-Each step is the whole call (for pc: the signal reset and the pipeline).
-Prints one JSON line with per-step CUDA-event times and GB/s (2 x input
-bytes / time).
+Each step is the whole call (for pc: the signal reset and the pipeline; for
+the collectives: metadata, push and wait).  Prints one JSON line with per-step
+CUDA-event times and GB/s (bytes read + bytes written / time).
+
+  python -m symmetric_memory_moe_gb300.profile_case --variant alltoall --tokens 4096
+  python -m symmetric_memory_moe_gb300.profile_case --variant allgather --bytes 33554432
 """
 from __future__ import annotations
 
@@ -15,8 +18,8 @@ import statistics
 
 import torch
 
-from . import abi
-from .torch_heap import CombineBuffers
+from . import abi, inputs
+from .torch_heap import CombineBuffers, TorchSymmHeap
 
 DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "int32": torch.int32,
           "uint8": torch.uint8}
@@ -25,7 +28,8 @@ DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "int32": torch.int32,
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--variant", default="pc",
-                    choices=["direct", "pc", "noalloc", "dispatch", "combine_back"])
+                    choices=["direct", "pc", "noalloc", "dispatch", "combine_back", "alltoall",
+                             "allgather"])
     ap.add_argument("--W", type=int, default=8)
     ap.add_argument("--S", type=int, default=256)
     ap.add_argument("--H", type=int, default=1)
@@ -39,7 +43,14 @@ def main(argv=None):
                     help="pc: 16-byte vector copies only (no bulk prefetch)")
     ap.add_argument("--bulk", action="store_true",
                     help="direct: bulk (TMA) copies through shared memory")
+    ap.add_argument("--tokens", type=int, default=4096, help="alltoall: tokens per PE")
+    ap.add_argument("--experts", type=int, default=256, help="alltoall: routed experts")
+    ap.add_argument("--topk", type=int, default=8, help="alltoall: experts per token")
+    ap.add_argument("--skew", type=float, default=1.0, help="alltoall: Zipf exponent")
+    ap.add_argument("--bytes", type=int, default=32 << 20, help="allgather: bytes per PE")
     args = ap.parse_args(argv)
+    if args.variant in ("alltoall", "allgather"):
+        return collective(args)
 
     dt = DTYPES[args.dtype]
     es = torch.empty((), dtype=dt).element_size()
@@ -88,6 +99,57 @@ def main(argv=None):
     moved = 2 * W * bufs.nbytes
     print(json.dumps({"variant": args.variant, "W": W, "S": S, "H": H, "D": D, "es": es,
                       "bytes_per_step": moved, "ms": [round(m, 4) for m in ms],
+                      "gbs_median": round(moved / (statistics.median(ms) * 1e-3) / 1e9, 1)}))
+    heap.close()
+
+
+def _time(step, steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for i in range(steps):
+        step()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+
+
+def collective(args):
+    W = args.W
+    ws = torch.empty(abi.shmem_collective_workspace(W) // 8, dtype=torch.int64, device="cuda")
+    if args.variant == "alltoall":
+        row = args.H * args.D * torch.empty((), dtype=DTYPES[args.dtype]).element_size()
+        counts = inputs.moe_counts(W, args.tokens, args.experts, args.topk, seed=5,
+                                   skew=args.skew)
+        in_rows, out_rows = int(counts.sum(1).max()), int(counts.sum(0).max())
+        heap = TorchSymmHeap(W, (in_rows + out_rows) * row + (4 << 20))
+        inp, out, sig = heap.malloc(in_rows * row), heap.malloc(out_rows * row), heap.malloc(64)
+        nin, moved = in_rows * row, 2 * int(counts.sum()) * row
+        dcounts = counts.cuda()
+
+        def step():
+            abi.shmem_alltoall(heap.handle, inp, out, dcounts.data_ptr(), W, row, in_rows,
+                               out_rows, ws.data_ptr(), sig)
+        shape = {"tokens": args.tokens, "experts": args.experts, "topk": args.topk,
+                 "skew": args.skew, "row_bytes": row, "rows": int(counts.sum())}
+    else:
+        n = args.bytes
+        heap = TorchSymmHeap(W, (W + 1) * n + (4 << 20))
+        inp, out, sig = heap.malloc(n), heap.malloc(W * n), heap.malloc(64)
+        nin, moved = n, W * n + W * W * n   # every input read once, W copies written
+
+        def step():
+            abi.shmem_allgather(heap.handle, inp, out, W, n, ws.data_ptr(), sig)
+        shape = {"bytes": n}
+    g = torch.Generator(device="cuda").manual_seed(7)
+    heap.views(inp, nin).copy_(torch.randint(0, 256, (W, nin), generator=g, dtype=torch.uint8,
+                                             device="cuda"))
+    _time(step, 3)
+    ms = _time(step, args.steps)
+    rc, info = abi.symm_check_error(heap.handle)
+    if rc != abi.SYMM_OK:
+        raise SystemExit(f"collective failed on the device: code {rc}, info {info}")
+    print(json.dumps({"variant": args.variant, "W": W, **shape, "bytes_per_step": moved,
+                      "ms": [round(m, 4) for m in ms],
                       "gbs_median": round(moved / (statistics.median(ms) * 1e-3) / 1e9, 1)}))
     heap.close()
 

@@ -92,6 +92,17 @@ def test_pc_workspace_sizes():
         abi.all2all_pc_workspace(8, 16, 1, 8, 2, 0, 0, 2)
 
 
+def test_collective_workspace_sizes():
+    # send/recv offsets and done counters (W*W each), receive totals (W), a flag
+    for W in (1, 2, 8, 100):
+        words = 3 * W * W + W + 1
+        assert abi.shmem_collective_workspace(W) == (words * 8 + 255) // 256 * 256
+    for W in (0, -1, 4097):
+        with pytest.raises(abi.SymmError) as e:
+            abi.shmem_collective_workspace(W)
+        assert e.value.code == abi.SYMM_EINVAL
+
+
 def test_validation_happens_before_any_launch():
     W, slab = 4, 8 << 20
     h = abi.symm_heap_init(FAKE_BASE, slab, W)
@@ -129,5 +140,21 @@ def test_validation_happens_before_any_launch():
         assert code(abi.shmem_signal_op, a + 4, 0, 1, 0, 0) == E              # misaligned
         assert code(abi.shmem_wait_for_signal, a, 0, 1, 3, 0) == E            # cmp 3
         assert code(abi.shmem_put_with_signal, a, 0, 0x1000, 0, 64, b, 0, 1, 5, 0) == E
+        # collectives: every check is on the host, before the metadata kernel
+        sig = abi.symm_malloc(h, 64)
+        ws, cnt = 0x10000, 0x20000   # plain device words, never touched here
+        assert code(abi.shmem_alltoall, a, b, None, W, 64, 8, 8, ws, sig) == E     # no counts
+        assert code(abi.shmem_alltoall, a, b, cnt, W - 1, 64, 8, 8, ws, sig) == E  # W != npes
+        assert code(abi.shmem_alltoall, a, b, cnt, W, 64, 8, 8, ws + 4, sig) == E  # workspace
+        assert code(abi.shmem_alltoall, a, b, cnt, W, 64, 8, 8, None, sig) == E
+        assert code(abi.shmem_alltoall, a, a + 8, cnt, W, 64, 8, 8, ws, sig) == E  # overlap
+        assert code(abi.shmem_alltoall, a, b, cnt, W, 64, 8, 8, ws, a) == E        # sig in `in`
+        assert code(abi.shmem_alltoall, a, b, cnt, W, 64, 8, 8, ws, sig + 4) == E  # misaligned
+        assert code(abi.shmem_alltoall, a, b, cnt, W, 1 << 20, 8, 8, ws, sig) == E  # past slab
+        assert code(abi.shmem_alltoall, a, b, cnt, W, 1 << 62, 8, 8, ws, sig) == E  # overflow
+        assert code(abi.shmem_allgather, a, b, W, 64, ws, None) == E
+        assert code(abi.shmem_allgather, a, b, W, n, ws, sig) == E                # out too small
+        assert code(abi.shmem_allgather, a, b, W, 1 << 62, ws, sig) == E
+        assert code(abi.shmem_allgather, a, b, W + 2, 64, ws, sig) == E
     finally:
         abi.symm_heap_destroy(h)
