@@ -206,6 +206,121 @@ int oracle_pc_replay(const void *in, void *out, int64_t W, int64_t S, int64_t H,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Sequential replay of the page's two-phase combine ("UDMA Optimized         */
+/* Implementation" with its "Wait/Notify Optimization": sections "Two-Phase   */
+/* Data Copy", "Symmetric Memory Layout" and "Dual Signal Memory Region       */
+/* Design").  Like the replay above it pins the combine's definition against */
+/* the page's own index arithmetic, here for the other staging layout:        */
+/*   peer memory per rank: W rank slots of [S][H][D]; slot r != rank receives */
+/*   rank r's whole segment for this rank (bulk, no buffering); slot rank     */
+/*   holds only the self-loop double buffer [buffer][block_s][H][D] at its    */
+/*   start.                                                                   */
+/*   signals per rank: region A [nbs][W] ("sender r has sent S block b",      */
+/*   written once, never reset), then region B [buffer][nbd*H] (self-loop     */
+/*   handshake: wait 0, write, notify 1; the consumer returns the credit by   */
+/*   setting 0), slots 8 int64 apart.                                        */
+/* Order per S block: every rank's bulk sends of that block, then every       */
+/* rank's self-loop tiles, then every rank's consumer tasks -- one legal      */
+/* interleaving of the concurrent kernel.  The bulk phase is replayed block   */
+/* by block, as the wait/notify version sends it (one send per S block and   */
+/* target, each followed by its region-A notify).  A wait whose condition     */
+/* does not hold in this order, or a region-A slot written twice, is a        */
+/* protocol error (returns -2).                                               */
+/*                                                                            */
+/* peer:    W * W*S*H*D * es bytes (rank-major)                               */
+/* signals: W * (nbs*W + buffer_num*nbd*H) * 8 int64 (rank-major), zeroed by  */
+/*          the caller first.                                                 */
+/* ------------------------------------------------------------------------ */
+int oracle_two_phase_replay(const void *in, void *out, int64_t W, int64_t S, int64_t H,
+                            int64_t D, int64_t es, int64_t block_s, int64_t block_d,
+                            int64_t buffer_num, void *peer_mem, int64_t *signals)
+{
+    /* The double buffer always fits slot rank: buffer buf holds S block buf
+     * (rows < S) while nbs <= buffer_num, and S > buffer_num*block_s after. */
+    if (W < 1 || S < 0 || H < 0 || D < 0 || es < 1 || block_s < 1 || block_d < 1 ||
+        buffer_num < 1)
+        return -1;
+    const unsigned char *a = (const unsigned char *)in;
+    unsigned char *c = (unsigned char *)out;
+    unsigned char *peer = (unsigned char *)peer_mem;
+    const int64_t nbs = (S + block_s - 1) / block_s;
+    const int64_t nbd = (D + block_d - 1) / block_d;
+    const int64_t row = H * D;                         /* one [H][D] row, elements */
+    const int64_t peer_rank_elems = W * S * row;
+    const int64_t tasks = nbd * H;                     /* self-loop tasks per block */
+    const int64_t region_b = nbs * W * 8;
+    const int64_t sig_rank_elems = region_b + buffer_num * tasks * 8;
+
+    for (int64_t bs = 0; bs < nbs; bs++) {
+        const int64_t buf = bs % buffer_num;
+        const int64_t s0 = bs * block_s;
+        const int64_t rows = (S - s0 < block_s) ? S - s0 : block_s;
+
+        /* phase 1: rank sends its rows target*S + s0 .. to the target's slot rank */
+        for (int64_t rank = 0; rank < W; rank++)
+            for (int64_t target = 0; target < W; target++) {
+                if (target == rank) continue;
+                const int64_t i_a = (rank * (S * W) + target * S + s0) * row;
+                const int64_t i_p = target * peer_rank_elems + (rank * S + s0) * row;
+                memcpy(peer + i_p * es, a + i_a * es, (size_t)(rows * row * es));
+                int64_t *slot = signals + target * sig_rank_elems + (bs * W + rank) * 8;
+                if (*slot != 0) return -2;             /* written once */
+                *slot = 1;
+            }
+
+        /* phase 2: self-loop tiles into the double buffer of slot rank */
+        for (int64_t rank = 0; rank < W; rank++)
+            for (int64_t task = 0; task < tasks; task++) {
+                const int64_t h = task % H;
+                const int64_t bd = task / H;
+                int64_t *slot = signals + rank * sig_rank_elems + region_b +
+                                (buf * tasks + task) * 8;
+                if (*slot != 0) return -2;             /* wait(slot == 0) */
+                for (int64_t i = 0; i < rows; i++)
+                    for (int64_t j = 0; j < block_d; j++) {
+                        const int64_t x = bd * block_d + j;
+                        if (x >= D) continue;          /* column mask */
+                        const int64_t i_a = ((rank * (S * W) + rank * S + s0 + i) * H + h) * D + x;
+                        const int64_t i_p = rank * peer_rank_elems + rank * S * row +
+                                            (buf * block_s + i) * row + h * D + x;
+                        memcpy(peer + i_p * es, a + i_a * es, (size_t)es);
+                    }
+                *slot = 1;                             /* notify after the fence */
+            }
+
+        /* consumers: every destination rank, every task (r, h, d block) */
+        for (int64_t rank = 0; rank < W; rank++)
+            for (int64_t task = 0; task < tasks * W; task++) {
+                const int64_t r = task % W;
+                const int64_t hd = task / W;           /* = block_d*H + h */
+                const int64_t h = hd % H;
+                const int64_t bd = hd / H;
+                int64_t *slot;
+                int64_t first_row;                     /* row of s0 inside slot r */
+                if (r == rank) {
+                    slot = signals + rank * sig_rank_elems + region_b + (buf * tasks + hd) * 8;
+                    first_row = buf * block_s;
+                } else {
+                    slot = signals + rank * sig_rank_elems + (bs * W + r) * 8;
+                    first_row = s0;
+                }
+                if (*slot != 1) return -2;             /* wait(slot == 1) */
+                for (int64_t i = 0; i < rows; i++)
+                    for (int64_t j = 0; j < block_d; j++) {
+                        const int64_t x = bd * block_d + j;
+                        if (x >= D) continue;
+                        const int64_t i_p = rank * peer_rank_elems + r * S * row +
+                                            (first_row + i) * row + h * D + x;
+                        const int64_t i_c = ((rank * S + s0 + i) * (H * W) + (r * H + h)) * D + x;
+                        memcpy(c + i_c * es, peer + i_p * es, (size_t)es);
+                    }
+                if (r == rank) *slot = 0;              /* credit return */
+            }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* One-sided primitives on a symmetric heap held in host memory.              */
 /* Source: "Distributed Architecture Design" section 5.3 (remote address =    */
 /* target PE's heap base + the pointer's offset from the local heap base),    */

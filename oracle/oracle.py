@@ -62,6 +62,8 @@ class Oracle:
         for name in ("oracle_put", "oracle_get", "oracle_signal_op", "oracle_wait_satisfied",
                      "oracle_put_with_signal"):
             getattr(lib, name).restype = ctypes.c_int
+        lib.oracle_two_phase_replay.argtypes = [_P, _P] + [_I64] * 8 + [_P, _P]
+        lib.oracle_two_phase_replay.restype = ctypes.c_int
         lib.oracle_alltoallv.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64]
         lib.oracle_alltoallv.restype = ctypes.c_int
         lib.oracle_allgather.argtypes = [_P, _P, _I64, _I64]
@@ -122,6 +124,25 @@ class Oracle:
         if rc:
             raise ValueError(f"oracle_pc_replay rc={rc}")
         return out, signals
+
+    def two_phase_replay(self, x: np.ndarray, W: int, S: int, H: int, D: int, block_s: int,
+                         block_d: int, buffer_num: int = 2):
+        """Sequential replay of the page's two-phase (bulk + self-loop) kernel.
+
+        Returns (out, peer_mem, signals_after): out is [W, S, H*W, D]; peer_mem
+        [W, W, S, H, D] (rank slots; slot d of PE d holds only the self-loop
+        double buffer at its start); signals [W, nbs*W + buffer_num*nbd*H, 8]."""
+        x = np.ascontiguousarray(x)
+        nbs, nbd = -(-S // block_s), -(-D // block_d)
+        out = np.empty((W, S, H * W, D), dtype=x.dtype)
+        peer = np.zeros((W, W, S, H, D), dtype=x.dtype)
+        signals = np.zeros((W, nbs * W + buffer_num * nbd * H, 8), np.int64)
+        rc = self.lib.oracle_two_phase_replay(self._ptr(x), self._ptr(out), W, S, H, D,
+                                              x.itemsize, block_s, block_d, buffer_num,
+                                              self._ptr(peer), self._ptr(signals))
+        if rc:
+            raise ValueError(f"oracle_two_phase_replay rc={rc}")
+        return out, peer, signals
 
     def alltoallv(self, x: np.ndarray, counts: np.ndarray, out_rows: int,
                   out: np.ndarray | None = None) -> np.ndarray:

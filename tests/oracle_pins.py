@@ -136,6 +136,32 @@ def pin_page_tile_loop(o):
         assert not sig.any()
 
 
+def pin_page_two_phase_loop(o):
+    """The sequential replay of the page's two-phase kernel (bulk rank slots,
+    self-loop double buffer, region A / region B signals) gives the (1, 2, 0,
+    3, 4) transpose; afterwards slot r of PE d holds PE r's rows d*S.. for
+    every r != d (the bulk arrives whole), every region-A slot of a sender
+    r != d reads 1 and its own slot 0, and every region-B slot is back at 0."""
+    cases = [((2, 4, 2, 8), 2, 8, 2), ((8, 16, 8, 128), 4, 64, 2), ((4, 40, 2, 999), 8, 256, 2),
+             ((3, 7, 1, 5), 2, 3, 3), ((5, 9, 2, 6), 4, 4, 1), ((1, 6, 3, 4), 2, 2, 2),
+             ((2, 3, 1, 7), 8, 16, 2)]
+    for (W, S, H, D), bs, bd, nbuf in cases:
+        x = _rand((W, S * W, H, D), 6, np.int16)
+        y, peer, sig = o.two_phase_replay(x, W, S, H, D, bs, bd, nbuf)
+        ref = x.reshape(W, W, S, H, D).transpose(1, 2, 0, 3, 4).reshape(W, S, W * H, D)
+        np.testing.assert_array_equal(y, ref)
+        nbs = -(-S // bs)
+        for d in range(W):
+            for r in range(W):
+                if r != d:
+                    np.testing.assert_array_equal(peer[d, r], x[r, d * S:(d + 1) * S])
+            region_a = sig[d, :nbs * W, 0].reshape(nbs, W)
+            want = np.ones((nbs, W), np.int64)
+            want[:, d] = 0
+            np.testing.assert_array_equal(region_a, want)
+            assert not sig[d, nbs * W:].any() and not sig[d, :, 1:].any()
+
+
 # -- bit patterns ----------------------------------------------------------
 def pin_bit_patterns(o):
     """Values move as raw bits: NaN payloads, -0 and infinities survive."""

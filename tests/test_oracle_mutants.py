@@ -46,6 +46,15 @@ MUTANTS = [
     ("oracle_alltoallv", "for (int64_t e = 0; e < d; e++)", "for (int64_t e = 0; e <= d; e++)",
      "off-by-one send offset"),
     ("oracle_allgather", "(d * W + r) * bytes", "(r * W + d) * bytes", "transposed gather"),
+    ("oracle_two_phase_replay", "(rank * S + s0) * row;", "(target * S + s0) * row;",
+     "bulk slot of the receiver"),
+    ("oracle_two_phase_replay", "first_row = buf * block_s;", "first_row = s0;",
+     "self buffer read as bulk"),
+    ("oracle_two_phase_replay", "(buf * block_s + i) * row + h * D + x;",
+     "(s0 + i) * row + h * D + x;", "self buffer written as bulk"),
+    ("oracle_two_phase_replay", "(bs * W + rank) * 8;", "(bs * W + target) * 8;",
+     "region-A slot of the receiver"),
+    ("oracle_two_phase_replay", "if (r == rank) *slot = 0;", ";", "no credit return"),
 ]
 
 
