@@ -227,6 +227,46 @@ int all2all_combine_host(symm_heap_t *heap, const void *host_in, void *host_out,
                          int tile_s, int block_d, int buffer_num, void *staging, int64_t *signals,
                          void *stream);
 
+/* ------------------------------------------------- two-phase combine -- */
+
+/* Workspace of all2all_combine_two_phase, per PE (allocate each with
+ * symm_malloc):
+ *   bulk    W rank slots of [S][H][D] (= the input's bytes);
+ *   signals region A, nbs*W slots (nbs = ceil(S / tile_s)), then region B,
+ *           buffer_num * nbd * H slots (nbd = ceil(D / block_d)), each slot
+ *           SYMM_SIGNAL_STRIDE_BYTES apart.
+ * block_d = 0 means D.  Errors: SYMM_EINVAL. */
+int all2all_two_phase_workspace(int W, int S, int H, int D, int elem_bytes, int tile_s,
+                                int block_d, int buffer_num, size_t *bulk_bytes,
+                                size_t *signal_bytes);
+
+/* [Reverse All2All (EP MoE Distributed Kernel), "UDMA Optimized
+ * Implementation" with its "Wait/Notify Optimization"]  The same combine as
+ * all2all_combine (out_d[s, r*H + h, x] = in_r[d*S + s, h, x]), in two phases:
+ *   phase 1  for every r != d, PE r's rows d*S .. d*S + S - 1 are sent in bulk
+ *            (S block by S block) to rank slot r of PE d's `bulk`, and each
+ *            arrived S block sets its region-A slot (b, r) of PE d to 1 once;
+ *   phase 2  PE d's own rows d*S .. go tile by tile (tile_s rows, block_d
+ *            elements) through the double buffer at the start of rank slot d
+ *            (buffer_num buffers), handshaking on region B (wait 0, write,
+ *            set 1; the consumer resets 0 after reading);
+ *   consumer PE d copies every tile from rank slot r (r != d) or from the
+ *            double buffer (r == d) into out_d.
+ * All W PEs run in one cooperative launch (preceded by an in-stream reset of
+ * the signals).  On return (in stream order), region A of every PE holds 1
+ * for each (block, r != d) and 0 for r == d, region B is all 0, and the bulk
+ * slots r != d hold the senders' segments.
+ * in, out: as for all2all_combine.  bulk, signals: from
+ * all2all_two_phase_workspace; no two of in/out/bulk/signals may overlap.
+ * Bulk (TMA) copies are used when H*D*elem_bytes and the in and bulk offsets
+ * are multiples of 16 bytes, 16-byte vector copies otherwise.
+ * Errors: SYMM_EINVAL (shapes, ranges, W != npes), SYMM_ECUDA (launch,
+ * including a grid the device cannot keep resident); a wait that gives up
+ * is reported by symm_check_error() as SYMM_ETIMEDOUT. */
+int all2all_combine_two_phase(symm_heap_t *heap, const void *in, void *out, int W, int S, int H,
+                              int D, int elem_bytes, int tile_s, int block_d, int buffer_num,
+                              void *bulk, int64_t *signals, void *stream);
+
 /* --------------------------------------------------------- collectives -- */
 
 /* Bytes of device workspace (plain device memory, 8-byte aligned; no need to

@@ -72,6 +72,8 @@ _SIGS = {
     "all2all_combine_host": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P],
     "all2all_combine_pc_noalloc": [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
     "shmem_collective_workspace": [_I, ctypes.POINTER(_SZ)],
+    "all2all_two_phase_workspace": [_I] * 8 + [ctypes.POINTER(_SZ)] * 2,
+    "all2all_combine_two_phase": [_P, _P, _P] + [_I] * 8 + [_P, _P, _P],
     "shmem_alltoall": [_P, _P, _P, _P, _I, _SZ, _SZ, _SZ, _P, _P, _P],
     "shmem_allgather": [_P, _P, _P, _I, _SZ, _P, _P, _P],
 }
@@ -239,6 +241,23 @@ def all2all_combine_pc_noalloc(heap, inp, out, W, S, H, D, elem_bytes, tile_s=16
     _check(lib().all2all_combine_pc_noalloc(heap, inp, out, W, S, H, D, elem_bytes, tile_s,
                                             block_d, buffer_num, _stream(stream)),
            "all2all_combine_pc_noalloc")
+
+
+# ------------------------------------------------------ two-phase combine --
+def all2all_two_phase_workspace(W, S, H, D, elem_bytes, tile_s=16, block_d=0, buffer_num=2):
+    """(bulk_bytes, signal_bytes) per PE."""
+    b, g = _SZ(0), _SZ(0)
+    _check(lib().all2all_two_phase_workspace(W, S, H, D, elem_bytes, tile_s, block_d, buffer_num,
+                                             ctypes.byref(b), ctypes.byref(g)),
+           "all2all_two_phase_workspace")
+    return b.value, g.value
+
+
+def all2all_combine_two_phase(heap, inp, out, W, S, H, D, elem_bytes, tile_s, block_d,
+                              buffer_num, bulk, signals, stream=None):
+    _check(lib().all2all_combine_two_phase(heap, inp, out, W, S, H, D, elem_bytes, tile_s,
+                                           block_d, buffer_num, bulk, signals, _stream(stream)),
+           "all2all_combine_two_phase")
 
 
 # ------------------------------------------------------------ collectives --

@@ -28,8 +28,8 @@ DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "int32": torch.int32,
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--variant", default="pc",
-                    choices=["direct", "pc", "noalloc", "dispatch", "combine_back", "alltoall",
-                             "allgather"])
+                    choices=["direct", "pc", "noalloc", "dispatch", "combine_back", "two_phase",
+                             "alltoall", "allgather"])
     ap.add_argument("--W", type=int, default=8)
     ap.add_argument("--S", type=int, default=256)
     ap.add_argument("--H", type=int, default=1)
@@ -51,6 +51,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.variant in ("alltoall", "allgather"):
         return collective(args)
+    if args.variant == "two_phase":
+        return two_phase(args)
 
     dt = DTYPES[args.dtype]
     es = torch.empty((), dtype=dt).element_size()
@@ -111,6 +113,34 @@ def _time(step, steps):
         ev[i + 1].record()
     torch.cuda.synchronize()
     return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+
+
+def two_phase(args):
+    W, S, H, D = args.W, args.S, args.H, args.D
+    es = torch.empty((), dtype=DTYPES[args.dtype]).element_size()
+    n = S * W * H * D * es
+    nb, ns = abi.all2all_two_phase_workspace(W, S, H, D, es, args.tile_s, args.block_d,
+                                             args.buffers)
+    heap = TorchSymmHeap(W, 2 * n + nb + ns + (4 << 20))
+    inp, out, bulk, sig = heap.malloc(n), heap.malloc(n), heap.malloc(nb), heap.malloc(ns)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    heap.views(inp, n).copy_(torch.randint(0, 256, (W, n), generator=g, dtype=torch.uint8,
+                                           device="cuda"))
+
+    def step():
+        abi.all2all_combine_two_phase(heap.handle, inp, out, W, S, H, D, es, args.tile_s,
+                                      args.block_d, args.buffers, bulk, sig)
+    _time(step, 3)
+    ms = _time(step, args.steps)
+    rc, info = abi.symm_check_error(heap.handle)
+    if rc != abi.SYMM_OK:
+        raise SystemExit(f"two-phase combine failed on the device: code {rc}, info {info}")
+    moved = 2 * W * n
+    print(json.dumps({"variant": "two_phase", "W": W, "S": S, "H": H, "D": D, "es": es,
+                      "tile_s": args.tile_s, "block_d": args.block_d, "buffers": args.buffers,
+                      "bytes_per_step": moved, "ms": [round(m, 4) for m in ms],
+                      "gbs_median": round(moved / (statistics.median(ms) * 1e-3) / 1e9, 1)}))
+    heap.close()
 
 
 def collective(args):

@@ -92,6 +92,19 @@ def test_pc_workspace_sizes():
         abi.all2all_pc_workspace(8, 16, 1, 8, 2, 0, 0, 2)
 
 
+def test_two_phase_workspace_sizes():
+    # bulk: W rank slots of [S][H][D]; signals: region A nbs*W + region B buffer_num*nbd*H slots
+    b, g = abi.all2all_two_phase_workspace(8, 2048, 1, 7168, 2, 16, 1024, 2)
+    assert b == 8 * 2048 * 7168 * 2 and g == (128 * 8 + 2 * 7 * 1) * 64
+    b, g = abi.all2all_two_phase_workspace(3, 7, 2, 5, 4, 2, 0, 3)   # block_d 0 = D
+    assert b == 3 * 7 * 2 * 5 * 4 and g == (4 * 3 + 3 * 1 * 2) * 64
+    for bad in [(0, 4, 1, 8, 2, 2, 0, 2), (2, 4, 1, 8, 0, 2, 0, 2), (2, 4, 1, 8, 2, 0, 0, 2),
+                (2, 4, 1, 8, 2, 2, -1, 2), (2, 4, 1, 8, 2, 2, 0, 0)]:
+        with pytest.raises(abi.SymmError) as e:
+            abi.all2all_two_phase_workspace(*bad)
+        assert e.value.code == abi.SYMM_EINVAL
+
+
 def test_collective_workspace_sizes():
     # send/recv offsets and done counters (W*W each), receive totals (W), a flag
     for W in (1, 2, 8, 100):
@@ -156,5 +169,17 @@ def test_validation_happens_before_any_launch():
         assert code(abi.shmem_allgather, a, b, W, n, ws, sig) == E                # out too small
         assert code(abi.shmem_allgather, a, b, W, 1 << 62, ws, sig) == E
         assert code(abi.shmem_allgather, a, b, W + 2, 64, ws, sig) == E
+        # two-phase combine: workspace ranges, overlaps, W, tiles
+        blk = abi.symm_malloc(h, n)
+        tsig = abi.symm_malloc(h, 4096)
+        tp = abi.all2all_combine_two_phase
+        assert code(tp, a, b, W + 1, 16, 2, 8, 2, 4, 0, 2, blk, tsig) == E   # W != npes
+        assert code(tp, a, b, W, 16, 2, 8, 2, 0, 0, 2, blk, tsig) == E       # tile_s 0
+        assert code(tp, a, b, W, 16, 2, 8, 2, 4, 0, 0, blk, tsig) == E       # no buffers
+        assert code(tp, a, b, W, 16, 2, 8, 2, 4, 0, 2, a, tsig) == E         # bulk is in
+        assert code(tp, a, b, W, 16, 2, 8, 2, 4, 0, 2, blk, blk) == E        # signals in bulk
+        assert code(tp, a, b, W, 16, 2, 8, 2, 4, 0, 2, blk, tsig + 4) == E   # misaligned
+        assert code(tp, a, b, W, 16, 2, 8, 2, 4, 0, 2, 0x1000, tsig) == E    # not in the heap
+        assert code(tp, a, a, W, 16, 2, 8, 2, 4, 0, 2, blk, tsig) == E       # in == out
     finally:
         abi.symm_heap_destroy(h)
