@@ -457,3 +457,53 @@ int oracle_allgather(const void *in, void *out, int64_t W, int64_t bytes)
             memcpy(dst + (d * W + r) * bytes, src + r * bytes, (size_t)bytes);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Fused AllGather + MatMul.                                                  */
+/* Source: HyperParallel RFC "Symmetric Memory", section 10                   */
+/* (fused_all_gather_matmul) and its example 2 (fused AllGather + MatMul):    */
+/* every rank r holds a_r (m_local x k) and its own b (k x n); the gathered   */
+/* gather_out (m_total x k, m_total = W * m_local) stacks a_0, a_1, ... in    */
+/* rank order, and the result on rank d is gather_out @ b_d (m_total x n).    */
+/* The section's formula also names a ReduceScatter, but the example's        */
+/* result is (m_total, n) on every rank: the plain reading, taken here, is    */
+/* the matmul of the gathered rows with no reduction.                         */
+/* Values are doubles (the caller widens fp16 / bf16 exactly); the sum runs   */
+/* over the k index in increasing order.                                      */
+/*   a [W][m_local][k], b [W][k][n] -> gather [W][m_total][k],                */
+/*   c [W][m_total][n]                                                        */
+/* ------------------------------------------------------------------------ */
+int oracle_ag_matmul(const double *a, const double *b, double *gather, double *c, int64_t W,
+                     int64_t m_local, int64_t k, int64_t n)
+{
+    if (W < 1 || m_local < 0 || k < 0 || n < 0)
+        return -1;
+    const int64_t m_total = W * m_local;
+    for (int64_t d = 0; d < W; d++)
+        for (int64_t r = 0; r < W; r++)
+            for (int64_t i = 0; i < m_local; i++)
+                for (int64_t x = 0; x < k; x++)
+                    gather[(d * m_total + r * m_local + i) * k + x] = a[(r * m_local + i) * k + x];
+    for (int64_t d = 0; d < W; d++)
+        for (int64_t i = 0; i < m_total; i++)
+            for (int64_t j = 0; j < n; j++) {
+                double acc = 0.0;
+                for (int64_t x = 0; x < k; x++)
+                    acc += gather[(d * m_total + i) * k + x] * b[(d * k + x) * n + j];
+                c[(d * m_total + i) * n + j] = acc;
+            }
+    return 0;
+}
+
+/* One output element c_d[i, j] of the same operation, straight from the     */
+/* inputs: row i of gather_out is row i % m_local of a_(i / m_local).         */
+double oracle_ag_matmul_at(const double *a, const double *b, int64_t W, int64_t m_local,
+                           int64_t k, int64_t n, int64_t d, int64_t i, int64_t j)
+{
+    const int64_t r = i / m_local, row = i % m_local;
+    double acc = 0.0;
+    for (int64_t x = 0; x < k; x++)
+        acc += a[(r * m_local + row) * k + x] * b[(d * k + x) * n + j];
+    (void)W;
+    return acc;
+}

@@ -68,6 +68,10 @@ class Oracle:
         lib.oracle_alltoallv.restype = ctypes.c_int
         lib.oracle_allgather.argtypes = [_P, _P, _I64, _I64]
         lib.oracle_allgather.restype = ctypes.c_int
+        lib.oracle_ag_matmul.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64]
+        lib.oracle_ag_matmul.restype = ctypes.c_int
+        lib.oracle_ag_matmul_at.argtypes = [_P, _P] + [_I64] * 7
+        lib.oracle_ag_matmul_at.restype = ctypes.c_double
         self.lib = lib
 
     # -- permutations ------------------------------------------------------
@@ -172,6 +176,31 @@ class Oracle:
         if rc:
             raise ValueError(f"oracle_allgather rc={rc}")
         return out
+
+    def ag_matmul(self, a: np.ndarray, b: np.ndarray):
+        """a: [W, m_local, k], b: [W, k, n] (any real dtype; widened to float64
+        exactly for fp16) -> (gather [W, W*m_local, k], c [W, W*m_local, n]),
+        float64."""
+        a = np.ascontiguousarray(a, dtype=np.float64)
+        b = np.ascontiguousarray(b, dtype=np.float64)
+        W, m_local, k = a.shape
+        n = b.shape[2]
+        assert b.shape == (W, k, n)
+        gather = np.empty((W, W * m_local, k), np.float64)
+        c = np.empty((W, W * m_local, n), np.float64)
+        rc = self.lib.oracle_ag_matmul(self._ptr(a), self._ptr(b), self._ptr(gather),
+                                       self._ptr(c), W, m_local, k, n)
+        if rc:
+            raise ValueError(f"oracle_ag_matmul rc={rc}")
+        return gather, c
+
+    def ag_matmul_at(self, a: np.ndarray, b: np.ndarray, d: int, i: int, j: int) -> float:
+        """c_d[i, j] alone (for sampled checks at full size); a, b float64."""
+        assert a.dtype == np.float64 and b.dtype == np.float64
+        assert a.flags["C_CONTIGUOUS"] and b.flags["C_CONTIGUOUS"]
+        W, m_local, k = a.shape
+        return self.lib.oracle_ag_matmul_at(self._ptr(a), self._ptr(b), W, m_local, k,
+                                            b.shape[2], d, i, j)
 
     # -- primitives on a host-memory heap -----------------------------------
     def put(self, heap: np.ndarray, slab: int, npes: int, target_off: int, src: np.ndarray,

@@ -308,6 +308,49 @@ def pin_allgather(o):
     assert o.allgather(x)[1].tolist() == [7, 8, 9, 10, 11, 12]
 
 
+def pin_ag_matmul_golden(o):
+    """Hand-worked W=2 values (golden/ag_matmul_w2.txt)."""
+    rows = {}
+    with open(os.path.join(HERE, "golden", "ag_matmul_w2.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                key, *vals = line.split()
+                rows.setdefault(key, []).append([float(v) for v in vals])
+    a = np.array([r[1:] for r in rows["a"]]).reshape(2, 1, 2)
+    b = np.array([r[1:] for r in rows["b"]]).reshape(2, 2, 2)
+    gather, c = o.ag_matmul(a, b)
+    for d in range(2):
+        np.testing.assert_array_equal(gather[d].reshape(-1), rows["gather"][0])
+    for d, *vals in rows["c"]:
+        np.testing.assert_array_equal(c[int(d)].reshape(-1), vals)
+        for i in range(2):
+            for j in range(2):
+                assert o.ag_matmul_at(a, b, int(d), i, j) == vals[i * 2 + j]
+
+
+def pin_ag_matmul_library(o):
+    """Small integer inputs (exact in float64): the gather is numpy's
+    concatenation of the ranks' rows, the result numpy's matmul of it with each
+    rank's b; one rank reduces to a plain matmul; the result is linear in b;
+    sampled single elements agree with the full result."""
+    rng = np.random.default_rng(41)
+    for W, m, k, n in [(1, 3, 4, 5), (2, 4, 3, 2), (3, 2, 5, 7), (4, 3, 8, 3)]:
+        a = rng.integers(-9, 10, (W, m, k)).astype(np.float64)
+        b1 = rng.integers(-9, 10, (W, k, n)).astype(np.float64)
+        b2 = rng.integers(-9, 10, (W, k, n)).astype(np.float64)
+        gather, c = o.ag_matmul(a, b1)
+        stacked = np.concatenate(list(a), axis=0)
+        for d in range(W):
+            np.testing.assert_array_equal(gather[d], stacked)
+            np.testing.assert_array_equal(c[d], np.matmul(stacked, b1[d]))
+        _, c2 = o.ag_matmul(a, b2)
+        _, c12 = o.ag_matmul(a, b1 + b2)
+        np.testing.assert_array_equal(c12, c + c2)
+        for _ in range(10):
+            d, i, j = rng.integers(0, W), rng.integers(0, W * m), rng.integers(0, n)
+            assert o.ag_matmul_at(a, b1, int(d), int(i), int(j)) == c[d, i, j]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

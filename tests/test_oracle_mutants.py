@@ -55,6 +55,13 @@ MUTANTS = [
     ("oracle_two_phase_replay", "(bs * W + rank) * 8;", "(bs * W + target) * 8;",
      "region-A slot of the receiver"),
     ("oracle_two_phase_replay", "if (r == rank) *slot = 0;", ";", "no credit return"),
+    ("oracle_ag_matmul", "gather[(d * m_total + r * m_local + i) * k + x]",
+     "gather[(d * m_total + d * m_local + i) * k + x]", "gather row of the receiver"),
+    ("oracle_ag_matmul", "b[(d * k + x) * n + j]", "b[(d * k + j) * n + x]", "transposed b"),
+    ("oracle_ag_matmul", "for (int64_t x = 0; x < k; x++)\n                    acc",
+     "for (int64_t x = 1; x < k; x++)\n                    acc", "dropped first k term"),
+    ("oracle_ag_matmul_at", "a[(r * m_local + row) * k + x]", "a[(d * m_local + row) * k + x]",
+     "sampled row from the receiver"),
 ]
 
 
