@@ -304,6 +304,40 @@ int shmem_alltoall(symm_heap_t *heap, const void *in, void *out, const int64_t *
 int shmem_allgather(symm_heap_t *heap, const void *in, void *out, int W, size_t bytes,
                     void *workspace, int64_t *signals, void *stream);
 
+/* ------------------------------------------ fused AllGather + MatMul -- */
+
+#define SYMM_DTYPE_F16 0
+#define SYMM_DTYPE_BF16 1
+
+/* Signal object of shmem_fused_all_gather_matmul, per PE (allocate with
+ * symm_malloc): W * m_local / block_size slots SYMM_SIGNAL_STRIDE_BYTES
+ * apart, followed by as many 8-byte counters (used on PE 0).  Errors:
+ * SYMM_EINVAL (shapes as for the call). */
+int shmem_fused_ag_matmul_workspace(int W, int m_local, int k, int n, int block_size,
+                                    size_t *signal_bytes);
+
+/* [RFC] 10 (fused_all_gather_matmul) and its example 2: every PE r holds a_r
+ * (m_local x k) and b_r (k x n), row-major, elements of `dtype`
+ * (SYMM_DTYPE_F16 or SYMM_DTYPE_BF16).  Computes, on every PE d,
+ *   gather_out_d = [a_0; a_1; ...; a_(W-1)]     (m_total x k, m_total = W*m_local)
+ *   c_d          = gather_out_d @ b_d           (m_total x n)
+ * with fp32 accumulation on the tensor cores and c rounded to `dtype`.  The
+ * rows are pushed in blocks of block_size rows; each block's signal slot
+ * (source r, block j) on PE d is set to 1 when it has arrived, and the
+ * matmul of the rows of that block starts as soon as its slot is set.  All W
+ * PEs run in one cooperative launch, preceded by an in-stream reset of the
+ * signals.
+ * Shapes: block_size must be 128 and m_local a multiple of it; k and n
+ * multiples of 8, at least 8.  a, b, c, gather_out, signals: symmetric
+ * objects, 16-byte aligned, pairwise disjoint; signals sized by
+ * shmem_fused_ag_matmul_workspace.
+ * Errors: SYMM_EINVAL (shapes, ranges, W != npes), SYMM_ECUDA (launch or
+ * tensor-map set-up); a wait that gives up is reported by symm_check_error()
+ * as SYMM_ETIMEDOUT. */
+int shmem_fused_all_gather_matmul(symm_heap_t *heap, const void *a, const void *b, void *c,
+                                  void *gather_out, int W, int m_local, int k, int n, int dtype,
+                                  int block_size, int64_t *signals, void *stream);
+
 /* ------------------------------------------- allocation-free variant -- */
 
 /* Size of the library's own static device array used by

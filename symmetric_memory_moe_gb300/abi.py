@@ -73,6 +73,8 @@ _SIGS = {
     "all2all_combine_pc_noalloc": [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
     "shmem_collective_workspace": [_I, ctypes.POINTER(_SZ)],
     "all2all_two_phase_workspace": [_I] * 8 + [ctypes.POINTER(_SZ)] * 2,
+    "shmem_fused_ag_matmul_workspace": [_I] * 5 + [ctypes.POINTER(_SZ)],
+    "shmem_fused_all_gather_matmul": [_P] * 5 + [_I] * 6 + [_P, _P],
     "all2all_combine_two_phase": [_P, _P, _P] + [_I] * 8 + [_P, _P, _P],
     "shmem_alltoall": [_P, _P, _P, _P, _I, _SZ, _SZ, _SZ, _P, _P, _P],
     "shmem_allgather": [_P, _P, _P, _I, _SZ, _P, _P, _P],
@@ -258,6 +260,26 @@ def all2all_combine_two_phase(heap, inp, out, W, S, H, D, elem_bytes, tile_s, bl
     _check(lib().all2all_combine_two_phase(heap, inp, out, W, S, H, D, elem_bytes, tile_s,
                                            block_d, buffer_num, bulk, signals, _stream(stream)),
            "all2all_combine_two_phase")
+
+
+# ---------------------------------------------- fused AllGather + MatMul --
+SYMM_DTYPE_F16 = 0
+SYMM_DTYPE_BF16 = 1
+
+
+def shmem_fused_ag_matmul_workspace(W, m_local, k, n, block_size=128):
+    """signal_bytes per PE."""
+    g = _SZ(0)
+    _check(lib().shmem_fused_ag_matmul_workspace(W, m_local, k, n, block_size, ctypes.byref(g)),
+           "shmem_fused_ag_matmul_workspace")
+    return g.value
+
+
+def shmem_fused_all_gather_matmul(heap, a, b, c, gather_out, W, m_local, k, n, dtype,
+                                  block_size, signals, stream=None):
+    _check(lib().shmem_fused_all_gather_matmul(heap, a, b, c, gather_out, W, m_local, k, n, dtype,
+                                               block_size, signals, _stream(stream)),
+           "shmem_fused_all_gather_matmul")
 
 
 # ------------------------------------------------------------ collectives --

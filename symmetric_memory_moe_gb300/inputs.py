@@ -143,3 +143,14 @@ def random_counts(W: int, high: int, seed: int, zero_frac: float = 0.0) -> torch
     if zero_frac > 0:
         c[torch.rand(W, W, generator=g) < zero_frac] = 0
     return c
+
+
+def ag_matmul_inputs(W: int, m_local: int, k: int, n: int, dtype: torch.dtype, seed: int):
+    """Per-rank a [W, m_local, k] and b [W, k, n] of the fused AllGather +
+    MatMul, N(0, 1) drawn in fp32 from one seeded generator (a first, then b)
+    and rounded to `dtype`."""
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    a = torch.randn(W, m_local, k, generator=g).to(dtype)
+    b = torch.randn(W, k, n, generator=g).to(dtype)
+    return a, b

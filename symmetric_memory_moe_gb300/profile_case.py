@@ -29,7 +29,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--variant", default="pc",
                     choices=["direct", "pc", "noalloc", "dispatch", "combine_back", "two_phase",
-                             "alltoall", "allgather"])
+                             "alltoall", "allgather", "ag_matmul"])
     ap.add_argument("--W", type=int, default=8)
     ap.add_argument("--S", type=int, default=256)
     ap.add_argument("--H", type=int, default=1)
@@ -48,11 +48,18 @@ def main(argv=None):
     ap.add_argument("--topk", type=int, default=8, help="alltoall: experts per token")
     ap.add_argument("--skew", type=float, default=1.0, help="alltoall: Zipf exponent")
     ap.add_argument("--bytes", type=int, default=32 << 20, help="allgather: bytes per PE")
+    ap.add_argument("--m-local", type=int, default=512, help="ag_matmul: rows per PE")
+    ap.add_argument("--k", type=int, default=1024, help="ag_matmul: inner dimension")
+    ap.add_argument("--n", type=int, default=2048, help="ag_matmul: columns of b")
+    ap.add_argument("--cublas", action="store_true",
+                    help="ag_matmul: also time torch.bmm on the gathered rows (context)")
     args = ap.parse_args(argv)
     if args.variant in ("alltoall", "allgather"):
         return collective(args)
     if args.variant == "two_phase":
         return two_phase(args)
+    if args.variant == "ag_matmul":
+        return ag_matmul(args)
 
     dt = DTYPES[args.dtype]
     es = torch.empty((), dtype=dt).element_size()
@@ -140,6 +147,40 @@ def two_phase(args):
                       "tile_s": args.tile_s, "block_d": args.block_d, "buffers": args.buffers,
                       "bytes_per_step": moved, "ms": [round(m, 4) for m in ms],
                       "gbs_median": round(moved / (statistics.median(ms) * 1e-3) / 1e9, 1)}))
+    heap.close()
+
+
+def ag_matmul(args):
+    W, m, k, n = args.W, args.m_local, args.k, args.n
+    dtype = {"bf16": torch.bfloat16, "fp16": torch.float16}[args.dtype]
+    code = abi.SYMM_DTYPE_BF16 if dtype == torch.bfloat16 else abi.SYMM_DTYPE_F16
+    sig_bytes = abi.shmem_fused_ag_matmul_workspace(W, m, k, n)
+    sizes = [m * k * 2, k * n * 2, W * m * n * 2, W * m * k * 2, sig_bytes]
+    heap = TorchSymmHeap(W, sum(sizes) + 256 * len(sizes) + (4 << 20))
+    pa, pb, pc, pg, ps = [heap.malloc(s) for s in sizes]
+    g = torch.Generator(device="cuda").manual_seed(7)
+    for p, nb in ((pa, sizes[0]), (pb, sizes[1])):
+        heap.views(p, nb).view(dtype).copy_(
+            torch.randn(W, nb // 2, generator=g, device="cuda").to(dtype))
+
+    def step():
+        abi.shmem_fused_all_gather_matmul(heap.handle, pa, pb, pc, pg, W, m, k, n, code, 128, ps)
+    _time(step, 3)
+    ms = _time(step, args.steps)
+    rc, info = abi.symm_check_error(heap.handle)
+    if rc != abi.SYMM_OK:
+        raise SystemExit(f"fused AllGather + MatMul failed on the device: code {rc}, info {info}")
+    flops = 2.0 * W * (W * m) * k * n
+    out = {"variant": "ag_matmul", "W": W, "m_local": m, "k": k, "n": n, "dtype": args.dtype,
+           "flops_per_step": flops, "ms": [round(x, 4) for x in ms],
+           "tflops_median": round(flops / (statistics.median(ms) * 1e-3) / 1e12, 1)}
+    if args.cublas:  # the same matmuls on already-gathered rows, by the library
+        A = torch.randn(W, W * m, k, generator=g, device="cuda").to(dtype)
+        B = torch.randn(W, k, n, generator=g, device="cuda").to(dtype)
+        _time(lambda: torch.bmm(A, B), 3)
+        cms = _time(lambda: torch.bmm(A, B), args.steps)
+        out["cublas_bmm_tflops_median"] = round(flops / (statistics.median(cms) * 1e-3) / 1e12, 1)
+    print(json.dumps(out))
     heap.close()
 
 

@@ -105,6 +105,18 @@ def test_two_phase_workspace_sizes():
         assert e.value.code == abi.SYMM_EINVAL
 
 
+def test_fused_ag_matmul_workspace_sizes():
+    # signals: W*m_local/128 slots of 64 B plus 8-byte counters
+    assert abi.shmem_fused_ag_matmul_workspace(8, 512, 1024, 2048) == 8 * 4 * (64 + 8)
+    for bad in [(0, 128, 64, 64), (2, 100, 64, 64), (2, 128, 60, 64), (2, 128, 64, 12),
+                (2, 128, 0, 64)]:
+        with pytest.raises(abi.SymmError) as e:
+            abi.shmem_fused_ag_matmul_workspace(*bad)
+        assert e.value.code == abi.SYMM_EINVAL
+    with pytest.raises(abi.SymmError):
+        abi.shmem_fused_ag_matmul_workspace(2, 128, 64, 64, 64)   # block_size != 128
+
+
 def test_collective_workspace_sizes():
     # send/recv offsets and done counters (W*W each), receive totals (W), a flag
     for W in (1, 2, 8, 100):
@@ -181,5 +193,17 @@ def test_validation_happens_before_any_launch():
         assert code(tp, a, b, W, 16, 2, 8, 2, 4, 0, 2, blk, tsig + 4) == E   # misaligned
         assert code(tp, a, b, W, 16, 2, 8, 2, 4, 0, 2, 0x1000, tsig) == E    # not in the heap
         assert code(tp, a, a, W, 16, 2, 8, 2, 4, 0, 2, blk, tsig) == E       # in == out
+        # fused AllGather + MatMul: W = 4, m_local 128, k 8, n 8 (2 KB a, 8 KB gather)
+        fa, fb, fc, fg, fs = [abi.symm_malloc(h, 16384) for _ in range(5)]
+        fm = abi.shmem_fused_all_gather_matmul
+        F16 = abi.SYMM_DTYPE_F16
+        assert code(fm, fa, fb, fc, fg, W, 128, 8, 8, 7, 128, fs) == E          # dtype
+        assert code(fm, fa, fb, fc, fg, W + 1, 128, 8, 8, F16, 128, fs) == E    # W
+        assert code(fm, fa, fb, fc, fg, W, 100, 8, 8, F16, 128, fs) == E        # m_local
+        assert code(fm, fa, fb, fc, fg, W, 128, 8, 8, F16, 64, fs) == E         # block
+        assert code(fm, fa, fb, fc, fa, W, 128, 8, 8, F16, 128, fs) == E        # overlap
+        assert code(fm, fa + 8, fb, fc, fg, W, 128, 8, 8, F16, 128, fs) == E    # alignment
+        assert code(fm, fa, fb, fc, 0x1000, W, 128, 8, 8, F16, 128, fs) == E   # not heap
+        assert code(fm, fa, fb, fc, fg, W, 128 * 16, 8, 8, F16, 128, fs) == E   # too big
     finally:
         abi.symm_heap_destroy(h)

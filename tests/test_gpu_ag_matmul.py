@@ -1,0 +1,117 @@
+"""GPU parity of the fused AllGather + MatMul (RFC "Symmetric Memory",
+section 10, example 2) against the oracle.
+
+gather_out must equal the stacked inputs bit for bit.  c is a floating-point
+contraction: the kernel multiplies fp16/bf16 inputs exactly, accumulates in
+fp32 on the tensor cores and rounds the result to the input type, so each
+element must lie within
+
+    u_out * |c_ref| + 2^-12 * sum_x |a_ix| |b_xj|
+
+of the oracle's fp64 value (u_out = 2^-11 for fp16, 2^-8 for bf16: the
+output rounding; 2^-12 bounds the fp32 accumulation over k <= 2^10 terms
+with room for a truncating adder, k * 2^-23 <= 2^-13).  Small shapes are
+checked on every element, the example's full size on sampled elements."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from symmetric_memory_moe_gb300 import abi, inputs
+from symmetric_memory_moe_gb300.torch_heap import TorchSymmHeap
+
+pytestmark = pytest.mark.gpu
+
+POISON = 0xA5
+DT = {"f16": (torch.float16, abi.SYMM_DTYPE_F16, 2.0 ** -11),
+      "bf16": (torch.bfloat16, abi.SYMM_DTYPE_BF16, 2.0 ** -8)}
+
+
+def run(W, m_local, k, n, dt, seed=0, repeat=1):
+    """Returns (a, b, gather [W, m_total, k] torch, c [W, m_total, n] float64 numpy,
+    signals [W, slots])."""
+    dtype, code, _ = DT[dt]
+    a, b = inputs.ag_matmul_inputs(W, m_local, k, n, dtype, seed)
+    m_total = W * m_local
+    sig_bytes = abi.shmem_fused_ag_matmul_workspace(W, m_local, k, n)
+    sizes = [a[0].numel() * 2, b[0].numel() * 2, m_total * n * 2, m_total * k * 2, sig_bytes]
+    heap = TorchSymmHeap(W, sum(sizes) + 256 * len(sizes) + (4 << 20))
+    try:
+        pa, pb, pc, pg, ps = [heap.malloc(s) for s in sizes]
+        heap.upload(pa, a.reshape(W, -1))
+        heap.upload(pb, b.reshape(W, -1))
+        heap.views(pc, sizes[2]).fill_(POISON)
+        heap.views(pg, sizes[3]).fill_(POISON)
+        for _ in range(repeat):
+            abi.shmem_fused_all_gather_matmul(heap.handle, pa, pb, pc, pg, W, m_local, k, n, code,
+                                              128, ps)
+        torch.cuda.synchronize()
+        rc, info = abi.symm_check_error(heap.handle)
+        assert rc == abi.SYMM_OK, (rc, info)
+        gather = heap.download(pg, sizes[3]).view(dtype).reshape(W, m_total, k)
+        c = heap.download(pc, sizes[2]).view(dtype).reshape(W, m_total, n).double().numpy()
+        sig = heap.download(ps, sig_bytes).view(torch.int64).reshape(W, -1)
+        return a, b, gather, c, sig[:, :W * (m_local // 128) * 8:8]
+    finally:
+        heap.close()
+
+
+def check_gather(a, gather):
+    W = a.shape[0]
+    stacked = a.reshape(W * a.shape[1], a.shape[2])
+    for d in range(W):
+        assert torch.equal(gather[d].view(torch.int16), stacked.view(torch.int16)), d
+
+
+@pytest.mark.parametrize("W,m_local,k,n,dt", [
+    (1, 128, 64, 256, "bf16"),     # one tile, one K slice
+    (1, 128, 256, 256, "f16"),
+    (2, 256, 320, 512, "bf16"),
+    (3, 128, 200, 264, "f16"),     # k and n not multiples of the tile
+    (4, 256, 72, 1000, "bf16"),
+])
+def test_small_shapes_every_element(W, m_local, k, n, dt):
+    o = oracle.load()
+    a, b, gather, c, sig = run(W, m_local, k, n, dt, seed=W * 10 + k)
+    check_gather(a, gather)
+    assert torch.equal(sig, torch.ones_like(sig))
+    a64, b64 = a.double().numpy(), b.double().numpy()
+    _, ref = o.ag_matmul(a64, b64)
+    _, mag = o.ag_matmul(np.abs(a64), np.abs(b64))
+    tol = DT[dt][2] * np.abs(ref) + 2.0 ** -12 * mag
+    err = np.abs(c - ref)
+    assert (err <= tol).all(), f"max err {err.max()}, worst ratio {(err / tol).max()}"
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_example_size_sampled(dt):
+    """The RFC example's shapes with 8 PEs: m_local 512, k 1024, n 2048,
+    blocks of 128 rows; 3000 sampled elements plus whole first and last rows."""
+    W, m_local, k, n = 8, 512, 1024, 2048
+    o = oracle.load()
+    a, b, gather, c, sig = run(W, m_local, k, n, dt, seed=7, repeat=2)
+    check_gather(a, gather)
+    assert torch.equal(sig, torch.ones_like(sig))
+    a64 = np.ascontiguousarray(a.double().numpy())
+    b64 = np.ascontiguousarray(b.double().numpy())
+    aa, ab = np.abs(a64), np.abs(b64)
+    rng = np.random.default_rng(3)
+    picks = [(int(rng.integers(W)), int(rng.integers(W * m_local)), int(rng.integers(n)))
+             for _ in range(3000)]
+    picks += [(d, i, j) for d in (0, W - 1) for i in (0, W * m_local - 1) for j in range(0, n, 97)]
+    for d, i, j in picks:
+        ref = o.ag_matmul_at(a64, b64, d, i, j)
+        tol = DT[dt][2] * abs(ref) + 2.0 ** -12 * o.ag_matmul_at(aa, ab, d, i, j)
+        assert abs(c[d, i, j] - ref) <= tol, (d, i, j, c[d, i, j], ref)
+
+
+def test_empty_rows_launch_nothing():
+    heap = TorchSymmHeap(2, 4 << 20)
+    try:
+        p = [heap.malloc(4096) for _ in range(5)]
+        abi.shmem_fused_all_gather_matmul(heap.handle, p[0], p[1], p[2], p[3], 2, 0, 64, 64,
+                                          abi.SYMM_DTYPE_F16, 128, p[4])
+        torch.cuda.synchronize()
+        assert abi.symm_check_error(heap.handle)[0] == abi.SYMM_OK
+    finally:
+        heap.close()
