@@ -12,7 +12,8 @@
 // matmul at once, 256 threads per CTA, one CTA per SM:
 //   warp 0      TMA producer: per output tile (PE d, 128 rows, 256 columns)
 //               it waits (acquire, bounded) for the signal of the 128-row
-//               block the tile reads, then streams 64-wide K slices of A
+//               block the tile reads (tiles of PE d's own rows read a_d and
+//               wait for nothing), then streams 64-wide K slices of A
 //               (the gathered rows, K-major) and B (b_d as stored: N-major,
 //               in 64-column boxes) into a 4-stage shared-memory ring,
 //               128-byte swizzled;
@@ -199,10 +200,13 @@ __device__ __forceinline__ int64_t* ag_counter(const AgArgs& a, uint32_t r, uint
 }
 
 // Output tile t: PE d, source rank r = (d + jr) % W, its 128-row block jb,
-// columns nt*kBN ..  Tiles of one block are consecutive, and every PE starts
-// with its own rows (jr = 0), block by block in push order.
+// columns nt*kBN ..  Tiles of one block are consecutive.  Every PE's own
+// rows (jr = 0) come first: they are read from a_d itself and wait for no
+// signal (the page's "start with local data"), while the push delivers the
+// other ranks' blocks, block by block in push order.
 struct AgTile {
   uint32_t d, r, jb, m0, n0;
+  bool self;
 };
 __device__ __forceinline__ AgTile ag_tile(const AgArgs& a, uint64_t t) {
   AgTile x;
@@ -210,8 +214,9 @@ __device__ __forceinline__ AgTile ag_tile(const AgArgs& a, uint64_t t) {
   uint64_t v = t / a.ntiles_n;
   x.d = (uint32_t)(v % a.W);
   v /= a.W;
-  const uint32_t jr = (uint32_t)(v % a.W);
-  x.jb = (uint32_t)(v / a.W);
+  x.jb = (uint32_t)(v % a.nblk);
+  const uint32_t jr = (uint32_t)(v / a.nblk);
+  x.self = jr == 0;
   x.r = (x.d + jr) % a.W;
   x.m0 = x.r * a.m_local + x.jb * kBM;
   x.n0 = nt * kBN;
@@ -231,8 +236,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 template <int FMT>
 __global__ void __launch_bounds__(kAgThreads, 1)
-    ag_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                   const AgArgs a) {
+    ag_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+                   const __grid_constant__ CUtensorMap tma_local,
+                   const __grid_constant__ CUtensorMap tma_b, const AgArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (symm::smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -269,8 +275,8 @@ __global__ void __launch_bounds__(kAgThreads, 1)
       bool ok = true;
       for (uint64_t t = blockIdx.x; ok && t < a.tiles; t += G) {
         const AgTile x = ag_tile(a, t);
-        if (symm::spin_wait(ag_signal(a, x.d, x.r, x.jb), symm::kCmpEq, 1, a.budget_ns, a.ctl,
-                            a.heap_base) != symm::kSpinOk) {
+        if (!x.self && symm::spin_wait(ag_signal(a, x.d, x.r, x.jb), symm::kCmpEq, 1, a.budget_ns,
+                                       a.ctl, a.heap_base) != symm::kSpinOk) {
           ok = false;
           break;
         }
@@ -284,7 +290,10 @@ __global__ void __launch_bounds__(kAgThreads, 1)
           }
           uint8_t* st = smem + (size_t)s * kStageBytes;
           symm::mbar_arrive_expect_tx(&full[s], kStageBytes);
-          tma_load_3d(st, &tma_a, (int)(kt * kBK), (int)x.m0, (int)x.d, &full[s]);
+          if (x.self)  // rows jb*128 .. of a_d itself
+            tma_load_3d(st, &tma_local, (int)(kt * kBK), (int)(x.jb * kBM), (int)x.d, &full[s]);
+          else
+            tma_load_3d(st, &tma_a, (int)(kt * kBK), (int)x.m0, (int)x.d, &full[s]);
           for (int i = 0; i < kBN / 64; ++i)  // b itself, row-major: 64 N x kBK K boxes
             tma_load_3d(st + kATile + i * (kBK * 128), &tma_b, (int)(x.n0 + 64 * i),
                         (int)(kt * kBK), (int)x.d, &full[s]);
@@ -552,8 +561,11 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   rc = ensure_ctrl(h, s);
   if (rc) return rc;
   const int fmt = dtype == SYMM_DTYPE_BF16 ? 1 : 0;
-  CUtensorMap map_a, map_b;
+  CUtensorMap map_a, map_local, map_b;
   rc = make_map(&map_a, h->base + off[3], fmt, (uint32_t)k, (uint32_t)(W * m_local), (uint32_t)W,
+                h->slab, kBK, kBM);
+  if (rc) return rc;
+  rc = make_map(&map_local, h->base + off[0], fmt, (uint32_t)k, (uint32_t)m_local, (uint32_t)W,
                 h->slab, kBK, kBM);
   if (rc) return rc;
   rc = make_map(&map_b, h->base + off[1], fmt, (uint32_t)n, (uint32_t)k, (uint32_t)W, h->slab, 64,
@@ -585,7 +597,7 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   args.ctl = reinterpret_cast<Control*>(h->base);
   args.heap_base = h->base;
   const int grid = (int)std::min<uint64_t>((uint64_t)cap, std::max<uint64_t>(args.tiles, 1));
-  void* kargs[] = {&map_a, &map_b, &args};
+  void* kargs[] = {&map_a, &map_local, &map_b, &args};
   const void* kfn = fmt ? (const void*)ag_gemm_kernel<1> : (const void*)ag_gemm_kernel<0>;
   return cuda_check(cudaLaunchCooperativeKernel(kfn, grid, kAgThreads, kargs, kAgSmem, s),
                     "shmem_fused_all_gather_matmul: launch");
