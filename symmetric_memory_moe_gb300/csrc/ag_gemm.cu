@@ -22,7 +22,8 @@
 //               (M 128, N 256, K 16) from the ring, committing each stage
 //               back to the producer and each finished tile to the epilogue;
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator (each warp its 32 TMEM
-//               lanes), rounding to the input type, stores to c_d; the other
+//               lanes), rounding to the input type, 128-byte-swizzled boxes
+//               in shared memory and TMA stores to c_d; the other
 //               accumulator is filled meanwhile;
 //   warps 6-7   push: 16 KB pieces of every rank's 128-row blocks, each read
 //               once and stored to all W PEs' gather_out; the warp that
@@ -64,7 +65,11 @@ constexpr uint32_t kBTile = kBN * kBK * 2;
 constexpr uint32_t kStageBytes = kATile + kBTile;
 constexpr int kAgThreads = 256;
 constexpr uint32_t kTmemCols = 2 * kBN;  // two accumulators of kBN fp32 columns
-constexpr size_t kAgSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+// epilogue staging: per epilogue warp two 32-row x 64-column output boxes
+// (4 KB each, 128-byte swizzled) for TMA stores
+constexpr uint32_t kOutBox = 32 * 64 * 2;
+constexpr uint32_t kOutBytes = 4 * 2 * kOutBox;
+constexpr size_t kAgSmem = 1024 + (size_t)kStages * kStageBytes + kOutBytes + 256;
 constexpr uint32_t kPushPiece = 16384;
 constexpr int kPushWarps = 2;
 constexpr int kPushUnroll = 4;
@@ -105,6 +110,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(symm::smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(symm::smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(symm::smem_addr(src))
       : "memory");
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -238,11 +251,13 @@ template <int FMT>
 __global__ void __launch_bounds__(kAgThreads, 1)
     ag_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                    const __grid_constant__ CUtensorMap tma_local,
-                   const __grid_constant__ CUtensorMap tma_b, const AgArgs a) {
+                   const __grid_constant__ CUtensorMap tma_b,
+                   const __grid_constant__ CUtensorMap tma_c, const AgArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (symm::smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint8_t* out_stage = smem + kStages * kStageBytes;  // 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + kOutBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -339,9 +354,15 @@ __global__ void __launch_bounds__(kAgThreads, 1)
       symm::mbar_wait(drain, 0, a.budget_ns);
     }
   } else if (warp < 6) {  // ------------------------------------ epilogue
-    const uint32_t q = (uint32_t)(warp & 3);  // TMEM lanes 32q .. 32q + 31
-    const uint32_t row_in_tile = 32 * q + lane;
-    uint64_t tc = 0;
+    // Each warp owns TMEM lanes 32q .. 32q + 31 (its 32 rows of the tile).
+    // Per 64-column chunk: two tcgen05.ld of 32 columns, rounding to the
+    // input type, 16-byte rows of a 128-byte-swizzled 32 x 64 box in this
+    // warp's shared staging (chunk j of row r at (j ^ (r & 7)) * 16), and
+    // one TMA store of the box (rows and columns past c's edge are
+    // dropped by the copy).  Two boxes per warp alternate.
+    const uint32_t q = (uint32_t)(warp & 3);
+    uint8_t* my_stage = out_stage + (size_t)q * 2 * kOutBox;
+    uint64_t tc = 0, chunks = 0;
     for (uint64_t t = blockIdx.x; t < a.tiles; t += G, ++tc) {
       const AgTile x = ag_tile(a, t);
       const uint32_t buf = (uint32_t)(tc & 1);
@@ -350,31 +371,42 @@ __global__ void __launch_bounds__(kAgThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t m_total = a.W * a.m_local;
-      const uint32_t row = x.m0 + row_in_tile;
-      uint8_t* crow = a.c + x.d * a.slab + ((size_t)row * a.n + x.n0) * 2;
 #pragma unroll 1
-      for (int ch = 0; ch < kBN / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + ((32 * q) << 16) + buf * kBN + ch * 32, v);
-        if (row < m_total) {
+      for (int ch = 0; ch < kBN / 64; ++ch, ++chunks) {
+        uint32_t v0[32], v1[32];
+        const uint32_t col = tmem + ((32 * q) << 16) + buf * kBN + ch * 64;
+        tmem_ld32(col, v0);
+        tmem_ld32(col + 32, v1);
+        if (ch == kBN / 64 - 1) {  // the accumulator is free for the next tile
+          tc_fence_before();
+          mbar_arrive(&tempty[buf]);
+        }
+        uint8_t* box = my_stage + (chunks & 1) * kOutBox;
+        if (chunks >= 2) {  // the store issued from this box two chunks ago has read it
+          if (lane == 0) symm::bulk_wait_read<1>();
+          __syncwarp();
+        }
+        uint8_t* row = box + lane * 128;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {  // 8 columns = one 16-byte store
-            const uint32_t col = x.n0 + ch * 32 + g * 8;
-            if (col < a.n) {
-              uint4 o;
-              o.x = pack2<FMT>(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
-              o.y = pack2<FMT>(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
-              o.z = pack2<FMT>(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
-              o.w = pack2<FMT>(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
-              symm::st16(crow + (ch * 32 + g * 8) * 2, o);
-            }
-          }
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t* vv = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+          uint4 o;
+          o.x = pack2<FMT>(__uint_as_float(vv[0]), __uint_as_float(vv[1]));
+          o.y = pack2<FMT>(__uint_as_float(vv[2]), __uint_as_float(vv[3]));
+          o.z = pack2<FMT>(__uint_as_float(vv[4]), __uint_as_float(vv[5]));
+          o.w = pack2<FMT>(__uint_as_float(vv[6]), __uint_as_float(vv[7]));
+          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = o;
+        }
+        symm::fence_proxy_async_shared();  // the box, for the async-proxy store
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tma_c, box, (int)(x.n0 + 64 * ch), (int)(x.m0 + 32 * q), (int)x.d);
+          symm::bulk_commit();
         }
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[buf]);
     }
+    if (lane == 0) symm::bulk_wait<0>();  // stores complete before the CTA leaves
+    __syncwarp();
   } else {  // ------------------------------------------------------ push
     const uint32_t block_bytes = kBM * a.k * 2;
     const uint32_t npieces = (block_bytes + kPushPiece - 1) / kPushPiece;
@@ -561,7 +593,7 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   rc = ensure_ctrl(h, s);
   if (rc) return rc;
   const int fmt = dtype == SYMM_DTYPE_BF16 ? 1 : 0;
-  CUtensorMap map_a, map_local, map_b;
+  CUtensorMap map_a, map_local, map_b, map_c;
   rc = make_map(&map_a, h->base + off[3], fmt, (uint32_t)k, (uint32_t)(W * m_local), (uint32_t)W,
                 h->slab, kBK, kBM);
   if (rc) return rc;
@@ -570,6 +602,9 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   if (rc) return rc;
   rc = make_map(&map_b, h->base + off[1], fmt, (uint32_t)n, (uint32_t)k, (uint32_t)W, h->slab, 64,
                 kBK);
+  if (rc) return rc;
+  rc = make_map(&map_c, h->base + off[2], fmt, (uint32_t)n, (uint32_t)(W * m_local), (uint32_t)W,
+                h->slab, 64, 32);
   if (rc) return rc;
   const int cap = ag_capacity(fmt);
   if (cap <= 0) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
@@ -597,7 +632,7 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   args.ctl = reinterpret_cast<Control*>(h->base);
   args.heap_base = h->base;
   const int grid = (int)std::min<uint64_t>((uint64_t)cap, std::max<uint64_t>(args.tiles, 1));
-  void* kargs[] = {&map_a, &map_local, &map_b, &args};
+  void* kargs[] = {&map_a, &map_local, &map_b, &map_c, &args};
   const void* kfn = fmt ? (const void*)ag_gemm_kernel<1> : (const void*)ag_gemm_kernel<0>;
   return cuda_check(cudaLaunchCooperativeKernel(kfn, grid, kAgThreads, kargs, kAgSmem, s),
                     "shmem_fused_all_gather_matmul: launch");
