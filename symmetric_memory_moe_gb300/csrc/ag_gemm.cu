@@ -63,7 +63,11 @@ constexpr int kStages = SYMM_AG_STAGES;
 constexpr uint32_t kATile = kBM * kBK * 2;
 constexpr uint32_t kBTile = kBN * kBK * 2;
 constexpr uint32_t kStageBytes = kATile + kBTile;
-constexpr int kAgThreads = 256;
+#ifndef SYMM_AG_PUSH_WARPS
+#define SYMM_AG_PUSH_WARPS 2
+#endif
+constexpr int kPushWarps = SYMM_AG_PUSH_WARPS;
+constexpr int kAgThreads = 32 * (6 + kPushWarps);  // TMA, MMA, 4 epilogue, push
 constexpr uint32_t kTmemCols = 2 * kBN;  // two accumulators of kBN fp32 columns
 // epilogue staging: per epilogue warp two 32-row x 64-column output boxes
 // (4 KB each, 128-byte swizzled) for TMA stores
@@ -71,7 +75,6 @@ constexpr uint32_t kOutBox = 32 * 64 * 2;
 constexpr uint32_t kOutBytes = 4 * 2 * kOutBox;
 constexpr size_t kAgSmem = 1024 + (size_t)kStages * kStageBytes + kOutBytes + 256;
 constexpr uint32_t kPushPiece = 16384;
-constexpr int kPushWarps = 2;
 constexpr int kPushUnroll = 4;
 
 struct AgArgs {
