@@ -83,11 +83,14 @@ def test_small_shapes_every_element(W, m_local, k, n, dt):
     assert (err <= tol).all(), f"max err {err.max()}, worst ratio {(err / tol).max()}"
 
 
-@pytest.mark.parametrize("dt", ["bf16", "f16"])
-def test_example_size_sampled(dt):
-    """The RFC example's shapes with 8 PEs: m_local 512, k 1024, n 2048,
-    blocks of 128 rows; 3000 sampled elements plus whole first and last rows."""
-    W, m_local, k, n = 8, 512, 1024, 2048
+@pytest.mark.parametrize("dt,W,m_local,k,n", [
+    ("bf16", 8, 512, 1024, 2048), ("f16", 8, 512, 1024, 2048),
+    ("bf16", 4, 256, 2048, 4096),   # 64 MB of b in all: the PE-major tile order
+])
+def test_example_size_sampled(dt, W, m_local, k, n):
+    """The RFC example's shapes with 8 PEs (m_local 512, k 1024, n 2048,
+    blocks of 128 rows), and a case whose b matrices do not fit in L2
+    together; 3000 sampled elements plus whole first and last rows."""
     o = oracle.load()
     a, b, gather, c, sig = run(W, m_local, k, n, dt, seed=7, repeat=2)
     check_gather(a, gather)
