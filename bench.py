@@ -383,7 +383,7 @@ def run_ours(args):
         "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": T, "d2h_bytes_per_step": T, "steps": e2e_steps,
                 "ms_per_step": round(e2e_ms, 3),
-                "call": "all2all_combine_host (pinned host buffers)"},
+                "call": "all2all_combine_host (pinned host buffers: the direct combine reads and writes them in place over the host link)"},
         "gpu_launches": args.steps * launches_per_step[args.variant],
         "clocks": sampler.summary(),
         "cpu_baseline": cpu,

@@ -217,11 +217,24 @@ int all2all_dispatch(symm_heap_t *heap, const void *in, void *out, int W, int S,
 int all2all_combine_back(symm_heap_t *heap, const void *in, void *out, int W, int Sp, int H,
                          int D, int elem_bytes, void *stream);
 
-/* all2all_combine on host buffers: copies host_in ([W][S*W][H][D],
- * contiguous) into the W input slabs, runs the combine, and copies the W
- * output slabs to host_out ([W][S][H*W][D]), all on `stream` with one
- * cudaMemcpyAsync per slab and direction.  Page-locked host buffers make the
- * copies asynchronous.  Returns once enqueued. */
+/* all2all_combine on host buffers: host_in ([W][S*W][H][D], contiguous) in,
+ * host_out ([W][S][H*W][D]) out.  For the direct variant with both buffers
+ * page-locked and mapped (cudaHostAlloc / torch pin_memory), each lying in
+ * one allocation, the combine kernel reads and writes them in place over
+ * the host link; `in`, `out`, staging and signals are then not used.
+ * Otherwise `in` and `out` (symmetric, S*W rows per PE each) are device
+ * space, and for S >= 16 the work is pipelined in 8
+ * chunks of S rows: each chunk's input rows are gathered into a compact
+ * buffer at the start of `in` (one 2-D copy per PE), combined into a buffer
+ * at the start of `out`, and copied out (one copy per PE), with two buffers
+ * alternating and the copies on two streams of the library's own, so that
+ * copies in, the combine and copies out of neighbouring chunks overlap.
+ * The caller's `stream` runs the combines and waits for the last copies, so
+ * work enqueued on it afterwards sees host_out complete.  After the call
+ * the device objects hold chunk buffers, not the whole input and output.
+ * Smaller S: one copy per slab and direction on `stream`.  Page-locked host
+ * buffers make the copies asynchronous.  Calls from several host threads
+ * are serialised while they enqueue.  Returns once enqueued. */
 int all2all_combine_host(symm_heap_t *heap, const void *host_in, void *host_out, const void *in,
                          void *out, int W, int S, int H, int D, int elem_bytes, int variant,
                          int tile_s, int block_d, int buffer_num, void *staging, int64_t *signals,

@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libsymm_a2a.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 SOURCES = ["heap.cu", "a2a.cu", "pc_noalloc.cu", "collectives.cu", "two_phase.cu",
-           "ag_gemm.cu"]
+           "ag_gemm.cu", "host_pipe.cu"]
 HEADERS = ["symm_device.cuh", "symm_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -87,8 +87,8 @@ constexpr int kPcMinBlocks = SYMM_PC_MIN_BLOCKS;
 template <bool INVERSE, bool ALIGNED>
 __global__ void __launch_bounds__(kRunThreads,
                                   ALIGNED ? SYMM_RUNS_MIN_BLOCKS : SYMM_RUNS_GENERAL_MIN_BLOCKS)
-    a2a_runs_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, size_t slab,
-                    uint32_t W, uint32_t Sb, size_t R, uint32_t nruns) {
+    a2a_runs_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, size_t in_pe,
+                    size_t out_pe, uint32_t W, uint32_t Sb, size_t R, uint32_t nruns) {
   const int lane = threadIdx.x & 31;
   const uint32_t warp = (blockIdx.x * kRunThreads + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * kRunThreads) >> 5;
@@ -97,12 +97,12 @@ __global__ void __launch_bounds__(kRunThreads,
     uint8_t* dst;
     if (!INVERSE) {
       const uint32_t r = k % W, t = k / W, s = t % Sb, d = t / Sb;
-      src = in + r * slab + (size_t)(d * Sb + s) * R;
-      dst = out + d * slab + (size_t)(s * W + r) * R;
+      src = in + r * in_pe + (size_t)(d * Sb + s) * R;
+      dst = out + d * out_pe + (size_t)(s * W + r) * R;
     } else {
       const uint32_t s = k % Sb, t = k / Sb, d = t % W, r = t / W;
-      src = in + d * slab + (size_t)(s * W + r) * R;
-      dst = out + r * slab + (size_t)(d * Sb + s) * R;
+      src = in + d * in_pe + (size_t)(s * W + r) * R;
+      dst = out + r * out_pe + (size_t)(d * Sb + s) * R;
     }
     if (ALIGNED)
       symm::warp_copy_aligned<SYMM_RUNS_UNROLL, symm::kRO, symm::kCS>(dst, src, R >> 4, lane);
@@ -468,7 +468,22 @@ int launch_runs(symm_heap* h, size_t in_off, size_t out_off, uint32_t W, uint32_
                                                               h->spin_budget, ctl);
     return cuda_check(cudaGetLastError(), what);
   }
-  const bool aligned = R % 16 == 0 && in_off % 16 == 0 && out_off % 16 == 0;
+  return symm_host::launch_runs_raw(in, out, h->slab, h->slab, W, Sb, R, inverse, s, what);
+}
+
+}  // namespace
+
+// The run permutation between any two device-accessible buffers: PE k's
+// input at in + k*in_pe, its output at out + k*out_pe (symmetric slabs, or
+// page-locked host memory reached over the host link).
+int symm_host::launch_runs_raw(const uint8_t* in, uint8_t* out, size_t in_pe, size_t out_pe,
+                               uint32_t W, uint32_t Sb, size_t R, bool inverse, cudaStream_t s,
+                               const char* what) {
+  const size_t nruns = (size_t)W * W * Sb;
+  if (nruns == 0 || R == 0) return SYMM_OK;
+  if (nruns > 0x7fffffffull) return fail(SYMM_EINVAL, std::string(what) + ": more than 2^31 runs");
+  const bool aligned = R % 16 == 0 && (uintptr_t)in % 16 == 0 && (uintptr_t)out % 16 == 0 &&
+                       in_pe % 16 == 0 && out_pe % 16 == 0;
   const void* kfn = inverse ? (aligned ? (const void*)a2a_runs_kernel<true, true>
                                        : (const void*)a2a_runs_kernel<true, false>)
                             : (aligned ? (const void*)a2a_runs_kernel<false, true>
@@ -479,17 +494,18 @@ int launch_runs(symm_heap* h, size_t in_off, size_t out_off, uint32_t W, uint32_
   const int grid = (int)(need < (size_t)cap ? need : (size_t)cap);
   const uint32_t n32 = (uint32_t)nruns;
   if (inverse && aligned)
-    a2a_runs_kernel<true, true><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R, n32);
+    a2a_runs_kernel<true, true><<<grid, kRunThreads, 0, s>>>(in, out, in_pe, out_pe, W, Sb, R, n32);
   else if (inverse)
-    a2a_runs_kernel<true, false><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R, n32);
+    a2a_runs_kernel<true, false><<<grid, kRunThreads, 0, s>>>(in, out, in_pe, out_pe, W, Sb, R,
+                                                             n32);
   else if (aligned)
-    a2a_runs_kernel<false, true><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R, n32);
+    a2a_runs_kernel<false, true><<<grid, kRunThreads, 0, s>>>(in, out, in_pe, out_pe, W, Sb, R,
+                                                             n32);
   else
-    a2a_runs_kernel<false, false><<<grid, kRunThreads, 0, s>>>(in, out, h->slab, W, Sb, R, n32);
+    a2a_runs_kernel<false, false><<<grid, kRunThreads, 0, s>>>(in, out, in_pe, out_pe, W, Sb, R,
+                                                              n32);
   return cuda_check(cudaGetLastError(), what);
 }
-
-}  // namespace
 
 // -------------------------------------------------------------- C ABI ---
 extern "C" int all2all_pc_workspace(int W, int S, int H, int D, int elem_bytes, int tile_s,
@@ -629,35 +645,3 @@ extern "C" int all2all_combine_back(symm_heap_t* h, const void* in, void* out, i
                      as_stream(stream), "all2all_combine_back");
 }
 
-extern "C" int all2all_combine_host(symm_heap_t* h, const void* host_in, void* host_out,
-                                    const void* in, void* out, int W, int S, int H, int D,
-                                    int elem_bytes, int variant, int tile_s, int block_d,
-                                    int buffer_num, void* staging, int64_t* signals,
-                                    void* stream) {
-  if (S < 0 || W < 1) return fail(SYMM_EINVAL, "all2all_combine_host: S < 0 or W < 1");
-  size_t in_off, out_off, nbytes;
-  int rc = check_perm(h, in, out, W, (size_t)S * W, H, D, elem_bytes, "all2all_combine_host",
-                      &in_off, &out_off, &nbytes);
-  if (rc) return rc;
-  if (nbytes && (!host_in || !host_out))
-    return fail(SYMM_EINVAL, "all2all_combine_host: NULL host buffer");
-  cudaStream_t s = as_stream(stream);
-  for (int r = 0; r < W && nbytes; ++r) {
-    rc = cuda_check(cudaMemcpyAsync(h->base + (size_t)r * h->slab + in_off,
-                                    static_cast<const uint8_t*>(host_in) + (size_t)r * nbytes,
-                                    nbytes, cudaMemcpyHostToDevice, s),
-                    "all2all_combine_host: host-to-device copy");
-    if (rc) return rc;
-  }
-  rc = all2all_combine(h, in, out, W, S, H, D, elem_bytes, variant, tile_s, block_d, buffer_num,
-                       staging, signals, stream);
-  if (rc) return rc;
-  for (int d = 0; d < W && nbytes; ++d) {
-    rc = cuda_check(cudaMemcpyAsync(static_cast<uint8_t*>(host_out) + (size_t)d * nbytes,
-                                    h->base + (size_t)d * h->slab + out_off, nbytes,
-                                    cudaMemcpyDeviceToHost, s),
-                    "all2all_combine_host: device-to-host copy");
-    if (rc) return rc;
-  }
-  return SYMM_OK;
-}

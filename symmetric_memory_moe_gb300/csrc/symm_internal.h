@@ -41,4 +41,9 @@ int sm_count();
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// The direct run permutation (combine when !inverse, its inverse otherwise)
+// between two device-accessible buffers with PE strides in_pe and out_pe.
+int launch_runs_raw(const uint8_t* in, uint8_t* out, size_t in_pe, size_t out_pe, uint32_t W,
+                    uint32_t Sb, size_t R, bool inverse, cudaStream_t s, const char* what);
+
 }  // namespace symm_host

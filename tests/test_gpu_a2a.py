@@ -214,18 +214,28 @@ def test_repeated_pc_calls_reuse_signals():
     assert_bits_equal(got, expect_combine(x, W, S, H, D))
 
 
-def test_host_buffer_entry_point():
-    """all2all_combine_host: host in -> device -> combine -> host out."""
-    W, S, H, D = 4, 16, 2, 24
-    x = _rand_bytes(W, S * W, H, D, 2, seed=9).view(torch.int16).reshape(W, S * W, H, D)
+@pytest.mark.parametrize("S", [10, 16, 37])
+def test_host_buffer_entry_point(S):
+    """all2all_combine_host: host in -> device -> combine -> host out.  S 10
+    takes the single-chunk path; S 16 and 37 the 8-chunk pipeline (37: a
+    ragged last chunk).  Two calls in a row with different inputs on the
+    same objects, pinned and (once) pageable host buffers."""
+    W, H, D = 4, 2, 24
     for variant, kind in (("direct", abi.SYMM_A2A_DIRECT), ("pc", abi.SYMM_A2A_PC)):
         bufs = CombineBuffers(W, S * W, H, D, 2, pc=variant == "pc", S=S, tile_s=4)
-        host_in = x.contiguous().pin_memory()
-        host_out = torch.full((W, S, H * W, D), -1, dtype=torch.int16).pin_memory()
-        abi.all2all_combine_host(bufs.heap.handle, host_in.data_ptr(), host_out.data_ptr(),
-                                 bufs.inp, bufs.out, W, S, H, D, 2, kind, 4, 0, 2, bufs.staging,
-                                 bufs.signals)
-        torch.cuda.synchronize()
-        want = expect_combine(x, W, S, H, D)
-        assert np.array_equal(host_out.view(torch.uint8).reshape(W, -1).numpy(), want)
+        for call in range(2):
+            x = _rand_bytes(W, S * W, H, D, 2, seed=9 + call + S).view(torch.int16)
+            x = x.reshape(W, S * W, H, D).contiguous()
+            pinned = not (variant == "direct" and call == 1)
+            host_in = x.pin_memory() if pinned else x.clone()
+            host_out = torch.full((W, S, H * W, D), -1, dtype=torch.int16)
+            if pinned:
+                host_out = host_out.pin_memory()
+            abi.all2all_combine_host(bufs.heap.handle, host_in.data_ptr(), host_out.data_ptr(),
+                                     bufs.inp, bufs.out, W, S, H, D, 2, kind, 4, 0, 2,
+                                     bufs.staging, bufs.signals)
+            torch.cuda.synchronize()
+            want = expect_combine(x, W, S, H, D)
+            assert np.array_equal(host_out.view(torch.uint8).reshape(W, -1).numpy(), want), \
+                (variant, call)
         bufs.heap.close()
