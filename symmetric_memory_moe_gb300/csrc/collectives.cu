@@ -34,6 +34,9 @@ using namespace symm_host;
 namespace {
 
 constexpr int kThreads = 256;
+#ifndef SYMM_AG_BCAST_UNROLL
+#define SYMM_AG_BCAST_UNROLL 8  // 16-byte vectors in flight per lane in the AllGather push
+#endif
 constexpr size_t kGatherPiece = 8192;  // AllGather work unit (bytes of one PE's input)
 enum { kErrRange = -5 };
 
@@ -218,7 +221,8 @@ __global__ void __launch_bounds__(kThreads)
     const int r = (int)(k / pieces);
     const size_t off = (size_t)(k % pieces) * kGatherPiece;
     const size_t len = bytes - off < kGatherPiece ? bytes - off : kGatherPiece;
-    warp_copy_bcast<4>(out + (size_t)r * bytes + off, slab, W, in + r * slab + off, len, lane);
+    warp_copy_bcast<SYMM_AG_BCAST_UNROLL>(out + (size_t)r * bytes + off, slab, W, in + r * slab + off,
+                                          len, lane);
     __syncwarp();
     int last = 0;
     if (lane == 0) last = (int64_t)atom_add_acq_rel_u64(&ws.done[r], 1) + 1 == pieces;
