@@ -202,7 +202,10 @@ __device__ __forceinline__ uint64_t sw128_mnmajor_desc(const void* tile) {
 
 __device__ __forceinline__ uint64_t atom_add_acq_rel_u64(uint64_t* p, uint64_t v) {
   uint64_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;"
+               : "=l"(old)
+               : "l"(p), "l"(v)
+               : "memory");
   return old;
 }
 
@@ -486,7 +489,8 @@ __global__ void ag_reset_kernel(uint8_t* signals, size_t slab, uint32_t W, uint3
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < (size_t)W * per_pe;
        i += (size_t)gridDim.x * blockDim.x)
     reinterpret_cast<int64_t*>(signals + (i / per_pe) * slab)[i % per_pe] = 0;
-  int64_t* counters = reinterpret_cast<int64_t*>(signals + (size_t)slots * SYMM_SIGNAL_STRIDE_BYTES);
+  int64_t* counters =
+      reinterpret_cast<int64_t*>(signals + (size_t)slots * SYMM_SIGNAL_STRIDE_BYTES);
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < slots;
        i += (size_t)gridDim.x * blockDim.x)
     counters[i] = 0;
@@ -535,7 +539,8 @@ struct AgShape {
 
 int ag_shape(int W, int m_local, int k, int n, int block_size, const char* what, AgShape* o) {
   if (W < 1 || W > 4096 || m_local < 0 || k < 1 || n < 1)
-    return fail(SYMM_EINVAL, std::string(what) + ": W outside [1, 4096], m_local < 0, k < 1 or n < 1");
+    return fail(SYMM_EINVAL,
+                std::string(what) + ": W outside [1, 4096], m_local < 0, k < 1 or n < 1");
   if (block_size != kBM)
     return fail(SYMM_EINVAL, std::string(what) + ": block_size must be 128 (the MMA tile height)");
   if (m_local % kBM)

@@ -267,10 +267,12 @@ __device__ __forceinline__ bool tp_tile(const TpArgs& a, const TpGroup& g, uint3
                                           (uint32_t)(len >> 4), g.gtid, g.nthreads);
   } else if (g.producer) {
     for (uint32_t i = g.gwarp; i < rows; i += g.nwarps)
-      symm::warp_copy<SYMM_TP_ROW_UNROLL, symm::kRO, symm::kST>(dst + i * dstride, src + i * sstride, len, lane);
+      symm::warp_copy<SYMM_TP_ROW_UNROLL, symm::kRO, symm::kST>(dst + i * dstride,
+                                                                src + i * sstride, len, lane);
   } else {
     for (uint32_t i = g.gwarp; i < rows; i += g.nwarps)
-      symm::warp_copy<SYMM_TP_ROW_UNROLL, symm::kCG, symm::kCS>(dst + i * dstride, src + i * sstride, len, lane);
+      symm::warp_copy<SYMM_TP_ROW_UNROLL, symm::kCG, symm::kCS>(dst + i * dstride,
+                                                                src + i * sstride, len, lane);
   }
   if (g.producer || self) {
     symm::group_sync(g.bar_id, g.nthreads);  // the group's copies precede the release
@@ -474,7 +476,8 @@ extern "C" int all2all_combine_two_phase(symm_heap_t* h, const void* in, void* o
   const int cap = tp_capacity(mode);
   if (cap <= 0) return fail(SYMM_ECUDA, std::string(what) + ": occupancy query failed");
   const size_t work = std::max<size_t>((size_t)sh.nbs * W * W * sh.nbd * H,
-                                       (size_t)sh.nbs * W * (W - 1) / (mode ? 1 : SYMM_TP_VEC_SENDERS));
+                                       (size_t)sh.nbs * W * (W - 1) /
+                                           (mode ? 1 : SYMM_TP_VEC_SENDERS));
   const int grid = (int)std::min<size_t>((size_t)cap, std::max<size_t>(work, 1));
   void* args[] = {&a};
   return cuda_check(cudaLaunchCooperativeKernel(tp_kernel(mode), grid, kTpThreads, args,
