@@ -56,7 +56,7 @@ constexpr int kTpThreads = 32 * kTpWarps;
 #define SYMM_TP_VEC_PRODUCERS 2
 #endif
 #ifndef SYMM_TP_ROW_UNROLL
-#define SYMM_TP_ROW_UNROLL 8
+#define SYMM_TP_ROW_UNROLL 4
 #endif
 template <bool BULK>
 struct TpRoles {
@@ -71,6 +71,9 @@ constexpr size_t kTpSmem = 128 + (size_t)kTpStages * kTpPiece;
 #define SYMM_TP_UNROLL 8
 #endif
 constexpr int kTpUnroll = SYMM_TP_UNROLL;  // vectors in flight per thread in a tile copy
+#ifndef SYMM_TP_ROW_MIN_BLOCKS  // CTAs per SM of the instances that copy by rows
+#define SYMM_TP_ROW_MIN_BLOCKS 2
+#endif
 #ifndef SYMM_TP_MIN_BLOCKS
 #define SYMM_TP_MIN_BLOCKS 1
 #endif
@@ -284,7 +287,8 @@ __device__ __forceinline__ bool tp_tile(const TpArgs& a, const TpGroup& g, uint3
 // BULK: sender chunks are 16-byte aligned (bulk copies); ALIGNED (implies
 // BULK): every tile row segment is too (group-wide vector tile copies).
 template <bool BULK, bool ALIGNED>
-__global__ void __launch_bounds__(kTpThreads, SYMM_TP_MIN_BLOCKS)
+__global__ void __launch_bounds__(kTpThreads,
+                                  ALIGNED ? SYMM_TP_MIN_BLOCKS : SYMM_TP_ROW_MIN_BLOCKS)
     a2a_two_phase_kernel(const TpArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int status[2][2];
