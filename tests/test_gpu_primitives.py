@@ -148,3 +148,33 @@ def test_pc_stale_signal_times_out_then_recovers():
     want = oracle.load().combine(x.numpy(), Wp, S, H, D).view(np.uint8).reshape(Wp, -1)
     assert np.array_equal(got, want)
     heap.close()
+
+
+def test_put_based_combine(heap):
+    """The combine composed from the primitives, in the RFC's push mode: PE r
+    puts every run it owes PE d (its rows d*S + s) into out_d's column r*H
+    with put_with_signal ADD 1 on d's counter; each PE then waits for its
+    counter to reach W*S.  The result equals the oracle's combine."""
+    o = oracle.load()
+    S, H, D, es = 6, 2, 12, 2
+    R = H * D * es
+    x = inputs.random_bytes(W * S * W * R, seed=21).view(W, S * W * R)
+    inp = heap.malloc(S * W * R)
+    out = heap.malloc(S * W * R)
+    sig = heap.malloc(64)
+    heap.upload(inp, x)
+    heap.views(out, S * W * R).fill_(0xA5)
+    heap.views(sig, 64).zero_()
+    for r in range(W):
+        src = abi.symm_at(heap.handle, inp, r)  # PE r's own input
+        for d in range(W):
+            for s in range(S):
+                abi.shmem_put_with_signal(heap.handle, out, (s * W + r) * R, src,
+                                          (d * S + s) * R, R, sig, 0, 1, abi.SYMM_SIGNAL_ADD, d)
+    for d in range(W):
+        abi.shmem_wait_for_signal(heap.handle, sig, 0, W * S, abi.SYMM_CMP_EQ, d)
+    torch.cuda.synchronize()
+    assert abi.symm_check_error(heap.handle)[0] == abi.SYMM_OK
+    want = o.combine(x.numpy().reshape(W, S * W, H, D * es), W, S, H, D * es)
+    assert np.array_equal(heap.download(out, S * W * R).numpy(),
+                          want.view(np.uint8).reshape(W, -1))
