@@ -69,6 +69,8 @@ def check_gather(a, gather):
     (2, 256, 320, 512, "bf16"),
     (3, 128, 200, 264, "f16"),     # k and n not multiples of the tile
     (4, 256, 72, 1000, "bf16"),
+    (2, 128, 8, 64, "f16"),        # the smallest k and n: zero-filled K slice, N boxes past n
+    (16, 128, 64, 256, "bf16"),    # 16 PEs
 ])
 def test_small_shapes_every_element(W, m_local, k, n, dt):
     o = oracle.load()
