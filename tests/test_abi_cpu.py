@@ -207,3 +207,14 @@ def test_validation_happens_before_any_launch():
         assert code(fm, fa, fb, fc, fg, W, 128 * 16, 8, 8, F16, 128, fs) == E   # too big
     finally:
         abi.symm_heap_destroy(h)
+
+
+def test_header_is_plain_c(tmp_path):
+    """The boundary header compiles as strict C99 (no C++ in the interface)."""
+    src = tmp_path / "use.c"
+    src.write_text('#include "symm_a2a.h"\n'
+                   "int main(void) { size_t b = 0; return shmem_collective_workspace(8, &b); }\n")
+    res = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                          "-fsyntax-only", "-I", os.path.join(ROOT, "include"), str(src)],
+                         capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
