@@ -185,17 +185,6 @@ extern "C" int all2all_combine_host(symm_heap_t* h, const void* host_in, void* h
       rc = cuda_check(cudaStreamWaitEvent(p->h2d, p->computed[b], 0), "all2all_combine_host");
       if (rc) return rc;
     }
-#ifdef SYMM_HOST_1D
-    for (int r = 0; r < W; ++r)
-      for (int d = 0; d < W; ++d) {
-        rc = cuda_check(cudaMemcpyAsync(h->base + (size_t)r * h->slab + in_off + boff +
-                                            (size_t)d * rows * R,
-                                        hin + r * nbytes + ((size_t)d * S + s0) * R,
-                                        (size_t)rows * R, cudaMemcpyHostToDevice, p->h2d),
-                        "all2all_combine_host: host-to-device copy");
-        if (rc) return rc;
-      }
-#else
     for (int r = 0; r < W; ++r) {
       rc = cuda_check(cudaMemcpy2DAsync(h->base + (size_t)r * h->slab + in_off + boff,
                                         (size_t)rows * R, hin + r * nbytes + (size_t)s0 * R,
@@ -204,7 +193,6 @@ extern "C" int all2all_combine_host(symm_heap_t* h, const void* host_in, void* h
                       "all2all_combine_host: host-to-device copy");
       if (rc) return rc;
     }
-#endif
     rc = cuda_check(cudaEventRecord(p->in_ready[b], p->h2d), "all2all_combine_host: event");
     if (rc) return rc;
     // (2) combine the chunk on the caller's stream
