@@ -29,6 +29,12 @@
 //               once and stored to all W PEs' gather_out; the warp that
 //               completes a block (acquire/release count) sets that block's
 //               signal on every PE.
+// When every PE's rows form an even number of 128-row blocks, the CTAs run
+// in two-CTA clusters: the pair computes the tiles of two row blocks that
+// share PE d and columns n0, each CTA loads half of every B slice and the
+// TMA multicast writes it into both CTAs' rings, so B is read from L2 once
+// per pair; a ring stage is refilled once both CTAs' MMAs have released it
+// (their commits arrive on both CTAs' barriers).
 // b is read in place (row-major k x n) as an MN-major operand.  Every wait
 // is bounded; a role that gives up
 // records the error, and the CTA drains its in-flight copies and MMAs before
@@ -67,6 +73,10 @@ constexpr uint32_t kStageBytes = kATile + kBTile;
 #define SYMM_AG_PUSH_WARPS 2
 #endif
 constexpr int kPushWarps = SYMM_AG_PUSH_WARPS;
+// CTAs per cluster sharing B slices (1 = no clusters)
+#ifndef SYMM_AG_CLUSTER
+#define SYMM_AG_CLUSTER 2
+#endif
 constexpr int kAgThreads = 32 * (6 + kPushWarps);  // TMA, MMA, 4 epilogue, push
 constexpr uint32_t kTmemCols = 2 * kBN;  // two accumulators of kBN fp32 columns
 // epilogue staging: per epilogue warp two 32-row x 64-column output boxes
@@ -116,6 +126,30 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(symm::smem_addr(bar))
       : "memory");
 }
+// The same box into the same shared-memory offset of every CTA in `mask`
+// (this cluster's CTAs), each completing `bytes` on its own barrier at the
+// offset of `bar`.
+__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int x, int y,
+                                               int z, uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(symm::smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(symm::smem_addr(bar)),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; orders what each did before.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
                                              int z) {
   asm volatile(
@@ -156,6 +190,14 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    symm::smem_addr(bar))
                : "memory");
+}
+// As tc_commit, arriving on the barrier at `bar`'s offset in every CTA of `mask`.
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(symm::smem_addr(bar)),
+      "h"(mask)
+      : "memory");
 }
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one row per lane).
 // The load and its wait are one asm statement, so no use of the registers
@@ -232,32 +274,41 @@ __device__ __forceinline__ int64_t* ag_counter(const AgArgs& a, uint32_t r, uint
 //                 stays in L2 while the row blocks stream past it (when the
 //                 b matrices do not fit, the first order re-reads them from
 //                 DRAM: 1010 against 1550 TFLOP/s at k = n = 4096).
+// With MC = 2 (two-CTA clusters) "jb" above stands for a pair of row blocks
+// (2 jb', 2 jb' + 1) and the pair's member is the fastest index: tiles 2P
+// and 2P + 1 share PE d and columns n0, so the cluster that runs them loads
+// each B slice once for both CTAs.
 struct AgTile {
   uint32_t d, r, jb, m0, n0;
   bool self;
 };
+template <int MC>
 __device__ __forceinline__ AgTile ag_tile(const AgArgs& a, uint64_t t) {
   AgTile x;
-  const uint64_t n_self = (uint64_t)a.W * a.nblk * a.ntiles_n;
+  const uint32_t member = (uint32_t)(t % MC);
+  t /= MC;
+  const uint32_t nb = a.nblk / MC;
+  const uint64_t n_self = (uint64_t)a.W * nb * a.ntiles_n;
   const bool self = t < n_self;
   uint64_t v = self ? t : t - n_self;
   const uint32_t nt = (uint32_t)(v % a.ntiles_n);
   v /= a.ntiles_n;
   uint32_t jr = 0;
   if (self) {  // (d, jb, nt)
-    x.jb = (uint32_t)(v % a.nblk);
-    x.d = (uint32_t)(v / a.nblk);
+    x.jb = (uint32_t)(v % nb);
+    x.d = (uint32_t)(v / nb);
   } else if (a.pe_major) {  // (d, jr - 1, jb, nt)
-    x.jb = (uint32_t)(v % a.nblk);
-    v /= a.nblk;
+    x.jb = (uint32_t)(v % nb);
+    v /= nb;
     jr = 1 + (uint32_t)(v % (a.W - 1));
     x.d = (uint32_t)(v / (a.W - 1));
   } else {  // (jr - 1, jb, d, nt)
     x.d = (uint32_t)(v % a.W);
     v /= a.W;
-    x.jb = (uint32_t)(v % a.nblk);
-    jr = 1 + (uint32_t)(v / a.nblk);
+    x.jb = (uint32_t)(v % nb);
+    jr = 1 + (uint32_t)(v / nb);
   }
+  x.jb = x.jb * MC + member;
   x.self = self;
   x.r = (x.d + jr) % a.W;
   x.m0 = x.r * a.m_local + x.jb * kBM;
@@ -276,7 +327,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-template <int FMT>
+template <int FMT, int MC>
 __global__ void __launch_bounds__(kAgThreads, 1)
     ag_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                    const __grid_constant__ CUtensorMap tma_local,
@@ -297,7 +348,7 @@ __global__ void __launch_bounds__(kAgThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       symm::mbar_init(&full[s], 1);
-      symm::mbar_init(&empty[s], 1);
+      symm::mbar_init(&empty[s], MC);  // freed by the MMA of every CTA that shares it
     }
     for (int b = 0; b < 2; ++b) {
       symm::mbar_init(&tfull[b], 1);
@@ -310,15 +361,16 @@ __global__ void __launch_bounds__(kAgThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (MC > 1) cluster_sync();  // the peer's barriers exist before anything lands in them
   const uint32_t tmem = *tmem_slot;
-  const uint32_t G = gridDim.x;
+  const uint32_t G = gridDim.x;  // a multiple of MC: a CTA keeps its pair member t % MC
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------- TMA producer
       uint64_t it = 0;
       bool ok = true;
       for (uint64_t t = blockIdx.x; ok && t < a.tiles; t += G) {
-        const AgTile x = ag_tile(a, t);
+        const AgTile x = ag_tile<MC>(a, t);
         if (!x.self && symm::spin_wait(ag_signal(a, x.d, x.r, x.jb), symm::kCmpEq, 1, a.budget_ns,
                                        a.ctl, a.heap_base) != symm::kSpinOk) {
           ok = false;
@@ -338,9 +390,17 @@ __global__ void __launch_bounds__(kAgThreads, 1)
             tma_load_3d(st, &tma_local, (int)(kt * kBK), (int)(x.jb * kBM), (int)x.d, &full[s]);
           else
             tma_load_3d(st, &tma_a, (int)(kt * kBK), (int)x.m0, (int)x.d, &full[s]);
-          for (int i = 0; i < kBN / 64; ++i)  // b itself, row-major: 64 N x kBK K boxes
-            tma_load_3d(st + kATile + i * (kBK * 128), &tma_b, (int)(x.n0 + 64 * i),
-                        (int)(kt * kBK), (int)x.d, &full[s]);
+          if (MC == 1) {
+            for (int i = 0; i < kBN / 64; ++i)  // b itself, row-major: 64 N x kBK K boxes
+              tma_load_3d(st + kATile + i * (kBK * 128), &tma_b, (int)(x.n0 + 64 * i),
+                          (int)(kt * kBK), (int)x.d, &full[s]);
+          } else {  // this CTA's share of the boxes, into both CTAs of the pair
+            constexpr int kShare = kBN / 64 / MC;
+            const int i0 = (int)cluster_rank() * kShare;
+            for (int i = i0; i < i0 + kShare; ++i)
+              tma_load_3d_mc(st + kATile + i * (kBK * 128), &tma_b, (int)(x.n0 + 64 * i),
+                             (int)(kt * kBK), (int)x.d, &full[s], (uint16_t)((1u << MC) - 1));
+          }
         }
       }
       // every load issued lands before the CTA may leave (bounded)
@@ -375,7 +435,10 @@ __global__ void __launch_bounds__(kAgThreads, 1)
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j)  // K = 16 per instruction (A: +32 bytes)
             tc_mma(acc, ad + 2 * j, bd + kBStep * j, idesc, (kt | j) != 0);
-          tc_commit(&empty[s]);
+          if (MC == 1)
+            tc_commit(&empty[s]);
+          else  // the stage is free once both CTAs' MMAs have read it
+            tc_commit_mc(&empty[s], (uint16_t)((1u << MC) - 1));
         }
         if (ok) tc_commit(&tfull[buf]);
       }
@@ -393,7 +456,7 @@ __global__ void __launch_bounds__(kAgThreads, 1)
     uint8_t* my_stage = out_stage + (size_t)q * 2 * kOutBox;
     uint64_t tc = 0, chunks = 0;
     for (uint64_t t = blockIdx.x; t < a.tiles; t += G, ++tc) {
-      const AgTile x = ag_tile(a, t);
+      const AgTile x = ag_tile<MC>(a, t);
       const uint32_t buf = (uint32_t)(tc & 1);
       if (!mbar_wait_ab(&tfull[buf], (uint32_t)((tc >> 1) & 1), a.budget_ns, a.ctl)) {
         symm::record_error(a.ctl, symm::kErrTimedOut, -6);
@@ -482,6 +545,9 @@ __global__ void __launch_bounds__(kAgThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // No CTA leaves while its peer may still deliver B boxes or MMA arrivals
+  // into its shared memory.
+  if (MC > 1) cluster_sync();
 }
 
 __global__ void ag_reset_kernel(uint8_t* signals, size_t slab, uint32_t W, uint32_t slots) {
@@ -560,14 +626,22 @@ int ag_shape(int W, int m_local, int k, int n, int block_size, const char* what,
   return SYMM_OK;
 }
 
-int ag_capacity(int fmt) {
+const void* ag_kernel(int fmt, int mc) {
+  if (mc == 2) return fmt ? (const void*)ag_gemm_kernel<1, 2> : (const void*)ag_gemm_kernel<0, 2>;
+  return fmt ? (const void*)ag_gemm_kernel<1, 1> : (const void*)ag_gemm_kernel<0, 1>;
+}
+
+// CTAs resident at once (one per SM: the kernel takes all of TMEM), in whole
+// clusters of mc CTAs.
+int ag_capacity(int fmt, int mc) {
   static std::mutex mu;
-  static int cached[2][64] = {};
+  static int cached[2][2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (cached[fmt][dev]) return cached[fmt][dev];
-  const void* k = fmt ? (const void*)ag_gemm_kernel<1> : (const void*)ag_gemm_kernel<0>;
+  int& slot = cached[fmt][mc - 1][dev];
+  if (slot) return slot;
+  const void* k = ag_kernel(fmt, mc);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAgSmem) !=
       cudaSuccess)
     return 0;
@@ -575,9 +649,25 @@ int ag_capacity(int fmt) {
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kAgThreads, kAgSmem) !=
       cudaSuccess)
     return 0;
-  // one CTA per SM: the kernel takes all of TMEM
-  cached[fmt][dev] = std::min(per_sm, 1) * sm_count();
-  return cached[fmt][dev];
+  int n = std::min(per_sm, 1) * sm_count();
+  if (mc > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(mc * std::max(n / mc, 1)));
+    cfg.blockDim = dim3(kAgThreads);
+    cfg.dynamicSmemBytes = kAgSmem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)mc;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess) return 0;
+    n = std::min(n, clusters * mc);
+  }
+  slot = n;
+  return slot;
 }
 
 }  // namespace
@@ -637,8 +727,11 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   rc = make_map(&map_c, h->base + off[2], fmt, (uint32_t)n, (uint32_t)(W * m_local), (uint32_t)W,
                 h->slab, 64, 32);
   if (rc) return rc;
-  const int cap = ag_capacity(fmt);
-  if (cap <= 0) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
+  // Two-CTA clusters sharing each B slice when the row blocks pair up (an
+  // even number per PE); single CTAs otherwise.
+  const int mc = SYMM_AG_CLUSTER > 1 && sh.nblk % 2 == 0 ? 2 : 1;
+  const int cap = ag_capacity(fmt, mc);
+  if (cap < mc) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
 
   ag_reset_kernel<<<(unsigned)std::min<size_t>(((size_t)W * sh.slots * 8 + 255) / 256 + 1, 1024),
                     256, 0, s>>>(h->base + off[4], h->slab, (uint32_t)W, sh.slots);
@@ -667,7 +760,31 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   args.heap_base = h->base;
   const int grid = (int)std::min<uint64_t>((uint64_t)cap, std::max<uint64_t>(args.tiles, 1));
   void* kargs[] = {&map_a, &map_local, &map_b, &map_c, &args};
-  const void* kfn = fmt ? (const void*)ag_gemm_kernel<1> : (const void*)ag_gemm_kernel<0>;
-  return cuda_check(cudaLaunchCooperativeKernel(kfn, grid, kAgThreads, kargs, kAgSmem, s),
-                    "shmem_fused_all_gather_matmul: launch");
+  // cooperative: every CTA resident at once, since tiles wait on blocks that
+  // other CTAs push
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(grid / mc * mc));
+  cfg.blockDim = dim3(kAgThreads);
+  cfg.dynamicSmemBytes = kAgSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeCooperative;
+  attrs[0].val.cooperative = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = (unsigned)mc;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = mc > 1 ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, ag_kernel(fmt, mc), kargs);
+  if (e != cudaSuccess && mc > 1) {
+    // a configuration the runtime refuses for clusters: single CTAs instead
+    (void)cudaGetLastError();
+    const int cap1 = ag_capacity(fmt, 1);
+    if (cap1 < 1) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
+    cfg.gridDim = dim3((unsigned)std::min<uint64_t>((uint64_t)cap1, args.tiles));
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, ag_kernel(fmt, 1), kargs);
+  }
+  return cuda_check(e, "shmem_fused_all_gather_matmul: launch");
 }
