@@ -34,7 +34,9 @@
 // share PE d and columns n0, each CTA loads half of every B slice and the
 // TMA multicast writes it into both CTAs' rings, so B is read from L2 once
 // per pair; a ring stage is refilled once both CTAs' MMAs have released it
-// (their commits arrive on both CTAs' barriers).
+// (their commits arrive on both CTAs' barriers).  The same code runs 2 x 2
+// clusters (A shared by the pairs of column tiles too) when built with
+// SYMM_AG_CLUSTER=4.
 // b is read in place (row-major k x n) as an MN-major operand.  Every wait
 // is bounded; a role that gives up
 // records the error, and the CTA drains its in-flight copies and MMAs before
@@ -73,7 +75,10 @@ constexpr uint32_t kStageBytes = kATile + kBTile;
 #define SYMM_AG_PUSH_WARPS 2
 #endif
 constexpr int kPushWarps = SYMM_AG_PUSH_WARPS;
-// CTAs per cluster sharing B slices (1 = no clusters)
+// Largest cluster to use: 1 (none), 2 (pairs sharing B) or 4 (2 x 2, pairs
+// sharing A as well).  Pairs measured fastest: on one GB300, RFC example /
+// k = n = 4096, 1193 / 1702 TFLOP/s against 1100 / 1638 for 2 x 2 and
+// 1155 / 1675 for single CTAs.
 #ifndef SYMM_AG_CLUSTER
 #define SYMM_AG_CLUSTER 2
 #endif
@@ -274,25 +279,26 @@ __device__ __forceinline__ int64_t* ag_counter(const AgArgs& a, uint32_t r, uint
 //                 stays in L2 while the row blocks stream past it (when the
 //                 b matrices do not fit, the first order re-reads them from
 //                 DRAM: 1010 against 1550 TFLOP/s at k = n = 4096).
-// With MC = 2 (two-CTA clusters) "jb" above stands for a pair of row blocks
-// (2 jb', 2 jb' + 1) and the pair's member is the fastest index: tiles 2P
-// and 2P + 1 share PE d and columns n0, so the cluster that runs them loads
-// each B slice once for both CTAs.
+// In clusters of CM x CN CTAs, "jb" above stands for a group of CM row blocks
+// and "nt" for a group of CN column tiles; the cluster's member index
+// cm + CM * cn (its rank) is the fastest index.  The CM CTAs with one cn
+// share PE d and columns n0 (one B slice), the CN CTAs with one cm share the
+// rows (one A slice).
 struct AgTile {
   uint32_t d, r, jb, m0, n0;
   bool self;
 };
-template <int MC>
+template <int CM, int CN>
 __device__ __forceinline__ AgTile ag_tile(const AgArgs& a, uint64_t t) {
   AgTile x;
-  const uint32_t member = (uint32_t)(t % MC);
-  t /= MC;
-  const uint32_t nb = a.nblk / MC;
-  const uint64_t n_self = (uint64_t)a.W * nb * a.ntiles_n;
+  const uint32_t member = (uint32_t)(t % (CM * CN));
+  t /= CM * CN;
+  const uint32_t nb = a.nblk / CM, ntn = a.ntiles_n / CN;
+  const uint64_t n_self = (uint64_t)a.W * nb * ntn;
   const bool self = t < n_self;
   uint64_t v = self ? t : t - n_self;
-  const uint32_t nt = (uint32_t)(v % a.ntiles_n);
-  v /= a.ntiles_n;
+  const uint32_t nt = (uint32_t)(v % ntn) * CN + member / CM;
+  v /= ntn;
   uint32_t jr = 0;
   if (self) {  // (d, jb, nt)
     x.jb = (uint32_t)(v % nb);
@@ -308,7 +314,7 @@ __device__ __forceinline__ AgTile ag_tile(const AgArgs& a, uint64_t t) {
     x.jb = (uint32_t)(v % nb);
     jr = 1 + (uint32_t)(v / nb);
   }
-  x.jb = x.jb * MC + member;
+  x.jb = x.jb * CM + member % CM;
   x.self = self;
   x.r = (x.d + jr) % a.W;
   x.m0 = x.r * a.m_local + x.jb * kBM;
@@ -327,7 +333,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-template <int FMT, int MC>
+template <int FMT, int CM, int CN>
 __global__ void __launch_bounds__(kAgThreads, 1)
     ag_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                    const __grid_constant__ CUtensorMap tma_local,
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(kAgThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       symm::mbar_init(&full[s], 1);
-      symm::mbar_init(&empty[s], MC);  // freed by the MMA of every CTA that shares it
+      symm::mbar_init(&empty[s], CM * CN);  // freed by the MMAs of the whole cluster
     }
     for (int b = 0; b < 2; ++b) {
       symm::mbar_init(&tfull[b], 1);
@@ -361,16 +367,20 @@ __global__ void __launch_bounds__(kAgThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (MC > 1) cluster_sync();  // the peer's barriers exist before anything lands in them
+  constexpr int MC = CM * CN;
+  constexpr uint16_t kAll = (uint16_t)((1u << MC) - 1);
+  const uint32_t rank = MC > 1 ? cluster_rank() : 0;
+  const uint32_t cm = rank % CM, cn = rank / CM;
+  if (MC > 1) cluster_sync();  // the peers' barriers exist before anything lands in them
   const uint32_t tmem = *tmem_slot;
-  const uint32_t G = gridDim.x;  // a multiple of MC: a CTA keeps its pair member t % MC
+  const uint32_t G = gridDim.x;  // a multiple of MC: a CTA keeps its member t % MC = rank
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------- TMA producer
       uint64_t it = 0;
       bool ok = true;
       for (uint64_t t = blockIdx.x; ok && t < a.tiles; t += G) {
-        const AgTile x = ag_tile<MC>(a, t);
+        const AgTile x = ag_tile<CM, CN>(a, t);
         if (!x.self && symm::spin_wait(ag_signal(a, x.d, x.r, x.jb), symm::kCmpEq, 1, a.budget_ns,
                                        a.ctl, a.heap_base) != symm::kSpinOk) {
           ok = false;
@@ -386,20 +396,31 @@ __global__ void __launch_bounds__(kAgThreads, 1)
           }
           uint8_t* st = smem + (size_t)s * kStageBytes;
           symm::mbar_arrive_expect_tx(&full[s], kStageBytes);
-          if (x.self)  // rows jb*128 .. of a_d itself
-            tma_load_3d(st, &tma_local, (int)(kt * kBK), (int)(x.jb * kBM), (int)x.d, &full[s]);
-          else
-            tma_load_3d(st, &tma_a, (int)(kt * kBK), (int)x.m0, (int)x.d, &full[s]);
-          if (MC == 1) {
-            for (int i = 0; i < kBN / 64; ++i)  // b itself, row-major: 64 N x kBK K boxes
+          // A: rows jb*128 .. of a_d itself (own rows) or of the gathered
+          // rows; with CN > 1 this CTA loads 128 / CN of them (the maps' box
+          // height) into every CTA of its row group
+          const CUtensorMap* amap = x.self ? &tma_local : &tma_a;
+          const int ay = (int)(x.self ? x.jb * kBM : x.m0);
+          if (CN == 1) {
+            tma_load_3d(st, amap, (int)(kt * kBK), ay, (int)x.d, &full[s]);
+          } else {
+            constexpr uint16_t kRowGroup = (uint16_t)(((1u << (CM * CN)) - 1) / ((1u << CM) - 1));
+            tma_load_3d_mc(st + cn * (kATile / CN), amap, (int)(kt * kBK),
+                           ay + (int)(cn * (kBM / CN)), (int)x.d, &full[s],
+                           (uint16_t)(kRowGroup << cm));
+          }
+          // B: b itself, row-major, in 64 N x kBK K boxes; with CM > 1 this
+          // CTA loads kBN / 64 / CM of them into every CTA of its column group
+          if (CM == 1) {
+            for (int i = 0; i < kBN / 64; ++i)
               tma_load_3d(st + kATile + i * (kBK * 128), &tma_b, (int)(x.n0 + 64 * i),
                           (int)(kt * kBK), (int)x.d, &full[s]);
-          } else {  // this CTA's share of the boxes, into both CTAs of the pair
-            constexpr int kShare = kBN / 64 / MC;
-            const int i0 = (int)cluster_rank() * kShare;
-            for (int i = i0; i < i0 + kShare; ++i)
+          } else {
+            constexpr int kShare = kBN / 64 / CM;
+            const uint16_t cols = (uint16_t)(((1u << CM) - 1) << (cn * CM));
+            for (int i = (int)cm * kShare; i < (int)(cm + 1) * kShare; ++i)
               tma_load_3d_mc(st + kATile + i * (kBK * 128), &tma_b, (int)(x.n0 + 64 * i),
-                             (int)(kt * kBK), (int)x.d, &full[s], (uint16_t)((1u << MC) - 1));
+                             (int)(kt * kBK), (int)x.d, &full[s], cols);
           }
         }
       }
@@ -438,7 +459,7 @@ __global__ void __launch_bounds__(kAgThreads, 1)
           if (MC == 1)
             tc_commit(&empty[s]);
           else  // the stage is free once both CTAs' MMAs have read it
-            tc_commit_mc(&empty[s], (uint16_t)((1u << MC) - 1));
+            tc_commit_mc(&empty[s], kAll);
         }
         if (ok) tc_commit(&tfull[buf]);
       }
@@ -456,7 +477,7 @@ __global__ void __launch_bounds__(kAgThreads, 1)
     uint8_t* my_stage = out_stage + (size_t)q * 2 * kOutBox;
     uint64_t tc = 0, chunks = 0;
     for (uint64_t t = blockIdx.x; t < a.tiles; t += G, ++tc) {
-      const AgTile x = ag_tile<MC>(a, t);
+      const AgTile x = ag_tile<CM, CN>(a, t);
       const uint32_t buf = (uint32_t)(tc & 1);
       if (!mbar_wait_ab(&tfull[buf], (uint32_t)((tc >> 1) & 1), a.budget_ns, a.ctl)) {
         symm::record_error(a.ctl, symm::kErrTimedOut, -6);
@@ -626,20 +647,24 @@ int ag_shape(int W, int m_local, int k, int n, int block_size, const char* what,
   return SYMM_OK;
 }
 
+// Cluster shapes: mc = 1 (single CTAs), 2 (CM 2 x CN 1: pairs sharing B),
+// 4 (CM 2 x CN 2: pairs sharing B, pairs sharing A).
 const void* ag_kernel(int fmt, int mc) {
-  if (mc == 2) return fmt ? (const void*)ag_gemm_kernel<1, 2> : (const void*)ag_gemm_kernel<0, 2>;
-  return fmt ? (const void*)ag_gemm_kernel<1, 1> : (const void*)ag_gemm_kernel<0, 1>;
+  if (mc == 4) return fmt ? (const void*)ag_gemm_kernel<1, 2, 2> : (const void*)ag_gemm_kernel<0, 2, 2>;
+  if (mc == 2) return fmt ? (const void*)ag_gemm_kernel<1, 2, 1> : (const void*)ag_gemm_kernel<0, 2, 1>;
+  return fmt ? (const void*)ag_gemm_kernel<1, 1, 1> : (const void*)ag_gemm_kernel<0, 1, 1>;
 }
+int ag_cn(int mc) { return mc == 4 ? 2 : 1; }
 
 // CTAs resident at once (one per SM: the kernel takes all of TMEM), in whole
 // clusters of mc CTAs.
 int ag_capacity(int fmt, int mc) {
   static std::mutex mu;
-  static int cached[2][2][64] = {};
+  static int cached[2][3][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  int& slot = cached[fmt][mc - 1][dev];
+  int& slot = cached[fmt][mc == 4 ? 2 : mc - 1][dev];
   if (slot) return slot;
   const void* k = ag_kernel(fmt, mc);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAgSmem) !=
@@ -714,12 +739,23 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   rc = ensure_ctrl(h, s);
   if (rc) return rc;
   const int fmt = dtype == SYMM_DTYPE_BF16 ? 1 : 0;
+  // Clusters when the row blocks pair up (an even number per PE), sharing A
+  // as well when the column tiles pair up; single CTAs otherwise.
+  const int ntn = (n + kBN - 1) / kBN;
+  int mc = 1;
+  if (SYMM_AG_CLUSTER >= 2 && sh.nblk % 2 == 0) mc = 2;
+  if (SYMM_AG_CLUSTER >= 4 && mc == 2 && ntn % 2 == 0) mc = 4;
   CUtensorMap map_a, map_local, map_b, map_c;
-  rc = make_map(&map_a, h->base + off[3], fmt, (uint32_t)k, (uint32_t)(W * m_local), (uint32_t)W,
-                h->slab, kBK, kBM);
-  if (rc) return rc;
-  rc = make_map(&map_local, h->base + off[0], fmt, (uint32_t)k, (uint32_t)m_local, (uint32_t)W,
-                h->slab, kBK, kBM);
+  // A boxes are kBM / CN rows high: each CTA of a row group loads its share
+  auto make_a_maps = [&](int cn) {
+    int r = make_map(&map_a, h->base + off[3], fmt, (uint32_t)k, (uint32_t)(W * m_local),
+                     (uint32_t)W, h->slab, kBK, (uint32_t)(kBM / cn));
+    if (!r)
+      r = make_map(&map_local, h->base + off[0], fmt, (uint32_t)k, (uint32_t)m_local, (uint32_t)W,
+                   h->slab, kBK, (uint32_t)(kBM / cn));
+    return r;
+  };
+  rc = make_a_maps(ag_cn(mc));
   if (rc) return rc;
   rc = make_map(&map_b, h->base + off[1], fmt, (uint32_t)n, (uint32_t)k, (uint32_t)W, h->slab, 64,
                 kBK);
@@ -727,9 +763,6 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   rc = make_map(&map_c, h->base + off[2], fmt, (uint32_t)n, (uint32_t)(W * m_local), (uint32_t)W,
                 h->slab, 64, 32);
   if (rc) return rc;
-  // Two-CTA clusters sharing each B slice when the row blocks pair up (an
-  // even number per PE); single CTAs otherwise.
-  const int mc = SYMM_AG_CLUSTER > 1 && sh.nblk % 2 == 0 ? 2 : 1;
   const int cap = ag_capacity(fmt, mc);
   if (cap < mc) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
 
@@ -782,6 +815,8 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
     (void)cudaGetLastError();
     const int cap1 = ag_capacity(fmt, 1);
     if (cap1 < 1) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
+    rc = make_a_maps(1);
+    if (rc) return rc;
     cfg.gridDim = dim3((unsigned)std::min<uint64_t>((uint64_t)cap1, args.tiles));
     cfg.numAttrs = 1;
     e = cudaLaunchKernelExC(&cfg, ag_kernel(fmt, 1), kargs);

@@ -71,6 +71,8 @@ def check_gather(a, gather):
     (4, 256, 72, 1000, "bf16"),
     (2, 128, 8, 64, "f16"),        # the smallest k and n: zero-filled K slice, N boxes past n
     (16, 128, 64, 256, "bf16"),    # 16 PEs
+    (2, 256, 128, 256, "f16"),     # row blocks pair up, one column tile: 2-CTA clusters
+    (3, 384, 64, 512, "bf16"),     # odd row blocks per PE: single CTAs
 ])
 def test_small_shapes_every_element(W, m_local, k, n, dt):
     o = oracle.load()
