@@ -113,7 +113,9 @@ void *symm_at(symm_heap_t *heap, const void *ptr, int pe);
 int symm_set_spin_budget(symm_heap_t *heap, uint64_t budget_ns);
 
 /* Synchronises `stream`, then returns the first device-side error recorded in
- * the heap header since the last check (SYMM_OK or SYMM_ETIMEDOUT) and clears
+ * the heap header since the last check (SYMM_OK; SYMM_ETIMEDOUT; SYMM_ERANGE
+ * from shmem_alltoall; SYMM_EINVAL from a cluster kernel launched without its
+ * cluster shape, which then did nothing) and clears
  * it.  Until it is cleared, every later device wait on this heap gives up at
  * once (the abort flag stays raised), so check after any launch that may
  * have timed out.  *info (optional) receives the byte offset from base of the signal that

@@ -333,12 +333,22 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// The kernel body for clusters of CM x CN CTAs (1 x 1: single CTAs).  The
+// tensor maps are the kernels' __grid_constant__ parameters.
 template <int FMT, int CM, int CN>
-__global__ void __launch_bounds__(kAgThreads, 1)
-    ag_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
-                   const __grid_constant__ CUtensorMap tma_local,
-                   const __grid_constant__ CUtensorMap tma_b,
-                   const __grid_constant__ CUtensorMap tma_c, const AgArgs a) {
+__device__ __forceinline__ void ag_gemm_body(const CUtensorMap& tma_a,
+                                             const CUtensorMap& tma_local,
+                                             const CUtensorMap& tma_b,
+                                             const CUtensorMap& tma_c, const AgArgs& a) {
+  constexpr int MC = CM * CN;
+  if (MC > 1) {  // a launch without this cluster shape gets an error, not multicasts
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    if (n != (uint32_t)MC || gridDim.x % MC) {
+      if (threadIdx.x == 0) symm::record_error(a.ctl, SYMM_EINVAL, (int64_t)n);
+      return;
+    }
+  }
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (symm::smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -367,7 +377,6 @@ __global__ void __launch_bounds__(kAgThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  constexpr int MC = CM * CN;
   constexpr uint16_t kAll = (uint16_t)((1u << MC) - 1);
   const uint32_t rank = MC > 1 ? cluster_rank() : 0;
   const uint32_t cm = rank % CM, cn = rank / CM;
@@ -424,9 +433,13 @@ __global__ void __launch_bounds__(kAgThreads, 1)
           }
         }
       }
-      // every load issued lands before the CTA may leave (bounded)
-      for (uint64_t i = it > (uint64_t)kStages ? it - kStages : 0; i < it; ++i)
+      // every load issued lands before the CTA may leave (bounded); in a
+      // cluster, so do the other CTAs' last releases of this CTA's stages
+      for (uint64_t i = it > (uint64_t)kStages ? it - kStages : 0; i < it; ++i) {
         symm::mbar_wait(&full[i % kStages], (uint32_t)((i / kStages) & 1), a.budget_ns);
+        if (MC > 1)
+          symm::mbar_wait(&empty[i % kStages], (uint32_t)((i / kStages) & 1), a.budget_ns);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {  // -------------------------------------- MMA issuer
@@ -571,6 +584,25 @@ __global__ void __launch_bounds__(kAgThreads, 1)
   if (MC > 1) cluster_sync();
 }
 
+template <int FMT>
+__global__ void __launch_bounds__(kAgThreads, 1)
+    ag_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+                   const __grid_constant__ CUtensorMap tma_local,
+                   const __grid_constant__ CUtensorMap tma_b,
+                   const __grid_constant__ CUtensorMap tma_c, const AgArgs a) {
+  ag_gemm_body<FMT, 1, 1>(tma_a, tma_local, tma_b, tma_c, a);
+}
+
+// The cluster shape is part of the kernel, so every launch of it has it.
+template <int FMT, int CM, int CN>
+__global__ void __cluster_dims__(CM * CN, 1, 1) __launch_bounds__(kAgThreads, 1)
+    ag_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tma_a,
+                           const __grid_constant__ CUtensorMap tma_local,
+                           const __grid_constant__ CUtensorMap tma_b,
+                           const __grid_constant__ CUtensorMap tma_c, const AgArgs a) {
+  ag_gemm_body<FMT, CM, CN>(tma_a, tma_local, tma_b, tma_c, a);
+}
+
 __global__ void ag_reset_kernel(uint8_t* signals, size_t slab, uint32_t W, uint32_t slots) {
   const size_t per_pe = (size_t)slots * (SYMM_SIGNAL_STRIDE_BYTES / 8);
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < (size_t)W * per_pe;
@@ -650,9 +682,13 @@ int ag_shape(int W, int m_local, int k, int n, int block_size, const char* what,
 // Cluster shapes: mc = 1 (single CTAs), 2 (CM 2 x CN 1: pairs sharing B),
 // 4 (CM 2 x CN 2: pairs sharing B, pairs sharing A).
 const void* ag_kernel(int fmt, int mc) {
-  if (mc == 4) return fmt ? (const void*)ag_gemm_kernel<1, 2, 2> : (const void*)ag_gemm_kernel<0, 2, 2>;
-  if (mc == 2) return fmt ? (const void*)ag_gemm_kernel<1, 2, 1> : (const void*)ag_gemm_kernel<0, 2, 1>;
-  return fmt ? (const void*)ag_gemm_kernel<1, 1, 1> : (const void*)ag_gemm_kernel<0, 1, 1>;
+  if (mc == 4)
+    return fmt ? (const void*)ag_gemm_cluster_kernel<1, 2, 2>
+               : (const void*)ag_gemm_cluster_kernel<0, 2, 2>;
+  if (mc == 2)
+    return fmt ? (const void*)ag_gemm_cluster_kernel<1, 2, 1>
+               : (const void*)ag_gemm_cluster_kernel<0, 2, 1>;
+  return fmt ? (const void*)ag_gemm_kernel<1> : (const void*)ag_gemm_kernel<0>;
 }
 int ag_cn(int mc) { return mc == 4 ? 2 : 1; }
 
@@ -794,32 +830,33 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   const int grid = (int)std::min<uint64_t>((uint64_t)cap, std::max<uint64_t>(args.tiles, 1));
   void* kargs[] = {&map_a, &map_local, &map_b, &map_c, &args};
   // cooperative: every CTA resident at once, since tiles wait on blocks that
-  // other CTAs push
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(grid / mc * mc));
-  cfg.blockDim = dim3(kAgThreads);
-  cfg.dynamicSmemBytes = kAgSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attrs[2];
-  attrs[0].id = cudaLaunchAttributeCooperative;
-  attrs[0].val.cooperative = 1;
-  attrs[1].id = cudaLaunchAttributeClusterDimension;
-  attrs[1].val.clusterDim.x = (unsigned)mc;
-  attrs[1].val.clusterDim.y = 1;
-  attrs[1].val.clusterDim.z = 1;
-  cfg.attrs = attrs;
-  cfg.numAttrs = mc > 1 ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelExC(&cfg, ag_kernel(fmt, mc), kargs);
-  if (e != cudaSuccess && mc > 1) {
-    // a configuration the runtime refuses for clusters: single CTAs instead
-    (void)cudaGetLastError();
-    const int cap1 = ag_capacity(fmt, 1);
-    if (cap1 < 1) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
-    rc = make_a_maps(1);
-    if (rc) return rc;
-    cfg.gridDim = dim3((unsigned)std::min<uint64_t>((uint64_t)cap1, args.tiles));
+  // other CTAs push (the cluster kernels carry their cluster shape)
+  cudaError_t e;
+  if (mc == 1) {
+    e = cudaLaunchCooperativeKernel(ag_kernel(fmt, 1), grid, kAgThreads, kargs, kAgSmem, s);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(grid / mc * mc));
+    cfg.blockDim = dim3(kAgThreads);
+    cfg.dynamicSmemBytes = kAgSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeCooperative;
+    attr.val.cooperative = 1;
+    cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelExC(&cfg, ag_kernel(fmt, 1), kargs);
+    e = cudaLaunchKernelExC(&cfg, ag_kernel(fmt, mc), kargs);
+    if (e != cudaSuccess) {
+      // a configuration the runtime refuses for clusters: single CTAs instead
+      (void)cudaGetLastError();
+      const int cap1 = ag_capacity(fmt, 1);
+      if (cap1 < 1) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
+      rc = make_a_maps(1);
+      if (rc) return rc;
+      e = cudaLaunchCooperativeKernel(ag_kernel(fmt, 1),
+                                      (int)std::min<uint64_t>((uint64_t)cap1, args.tiles),
+                                      kAgThreads, kargs, kAgSmem, s);
+    }
   }
   return cuda_check(e, "shmem_fused_all_gather_matmul: launch");
 }

@@ -254,6 +254,9 @@ extern "C" int symm_check_error(symm_heap_t* h, void* stream, int64_t* info) {
   const int code = ctl.error ? ctl.error : SYMM_ETIMEDOUT;
   if (code == SYMM_ERANGE)
     return fail(code, "device-side sizes exceed a buffer (nothing was copied)");
+  if (code == SYMM_EINVAL)
+    return fail(code, "a kernel found itself launched without the cluster shape it was built "
+                      "for (clusters of " + std::to_string(ctl.error_info) + " CTAs); it did nothing");
   return fail(code, "device wait gave up (signal at heap byte offset " +
                         std::to_string(ctl.error_info) + ")");
 }
