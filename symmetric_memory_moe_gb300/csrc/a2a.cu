@@ -68,6 +68,11 @@ namespace {
 #ifndef SYMM_PC_UNROLL
 #define SYMM_PC_UNROLL 4
 #endif
+// 16-byte vectors in flight per thread in the producer/consumer tile copies
+// that spread a whole tile over the group (tiles with 16-byte-aligned rows)
+#ifndef SYMM_PC_FLAT_UNROLL
+#define SYMM_PC_FLAT_UNROLL 4
+#endif
 #ifndef SYMM_PC_MIN_BLOCKS
 #define SYMM_PC_MIN_BLOCKS 3
 #endif
@@ -210,6 +215,33 @@ struct PcArgs {
   const uint8_t* heap_base;
 };
 
+// One tile (rows x vrow 16-byte vectors, rows dst_row / src_row bytes apart)
+// copied by a 128-thread group with the tile flattened to vectors, so narrow
+// rows still keep every thread busy; U vectors in flight per thread.  Offsets
+// inside the tile are 32-bit (the host allows this copy only for tiles whose
+// rows span less than 4 GiB).
+template <int U, symm::LoadKind LK, symm::StoreKind SK>
+__device__ __forceinline__ void group_copy_tile(uint8_t* dst, uint32_t dst_row,
+                                                const uint8_t* src, uint32_t src_row,
+                                                uint32_t rows, uint32_t vrow, int gtid) {
+  const uint32_t nv = rows * vrow;
+  for (uint32_t v0 = gtid; v0 < nv; v0 += kPcGroup * U) {
+    uint4 x[U];
+    uint32_t off_s[U], off_d[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t v = v0 + u * kPcGroup;
+      const uint32_t i = v / vrow, c = v - i * vrow;
+      off_s[u] = i * src_row + 16 * c;
+      off_d[u] = i * dst_row + 16 * c;
+      if (v < nv) x[u] = symm::ld16<LK>(src + off_s[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (v0 + u * kPcGroup < nv) symm::st16k<SK>(dst + off_d[u], x[u]);
+  }
+}
+
 // Input rows of one producer task (tile of S block b, slot q), for the
 // bulk prefetch: q = blockIdx.x + j*gridDim.x is the CTA's j-th slot.
 struct PcTile {
@@ -255,7 +287,10 @@ __device__ __forceinline__ void pc_prefetch(const PcArgs& a, uint32_t nq, uint64
 constexpr int kPcPrefetch = SYMM_PC_PREFETCH;
 constexpr uint32_t kPcMaxPrefetchTile = 32 * 1024;
 
-template <bool PREFETCH>
+// FLAT: every tile row, base and row stride is 16-byte aligned and a tile
+// spans less than 4 GiB, so whole tiles are copied by group_copy_tile;
+// otherwise row by row with warp_copy (any alignment).
+template <bool PREFETCH, bool FLAT>
 __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
     a2a_pc_kernel(const PcArgs a, uint32_t tile_bytes) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -345,16 +380,26 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
         const uint8_t* src =
             a.in + r * a.slab + (((size_t)(d * a.S + s0) * a.H + h) * a.D + x0) * a.es;
         const size_t src_row = (size_t)a.H * a.D * a.es;
-        for (uint32_t i = gwarp; i < rows; i += 4)
-          symm::warp_copy<SYMM_PC_UNROLL, symm::kRO, symm::kST>(stage + i * stage_row,
-                                                                 src + i * src_row, len, lane);
+        if (FLAT)
+          group_copy_tile<SYMM_PC_FLAT_UNROLL, symm::kRO, symm::kST>(
+              stage, (uint32_t)stage_row, src, (uint32_t)src_row, rows, (uint32_t)(len >> 4),
+              gtid);
+        else
+          for (uint32_t i = gwarp; i < rows; i += 4)
+            symm::warp_copy<SYMM_PC_UNROLL, symm::kRO, symm::kST>(stage + i * stage_row,
+                                                                   src + i * src_row, len, lane);
       }
     } else {
       // consumer: staged tile -> output rows s0 + i, column r*H + h
       uint8_t* dst = a.out + d * a.slab + ((size_t)s0 * a.H * a.W * a.D) * a.es + stage_col;
-      for (uint32_t i = gwarp; i < rows; i += 4)
-        symm::warp_copy<SYMM_PC_UNROLL, symm::kCG, symm::kCS>(dst + i * stage_row,
-                                                               stage + i * stage_row, len, lane);
+      if (FLAT)
+        group_copy_tile<SYMM_PC_FLAT_UNROLL, symm::kCG, symm::kCS>(
+            dst, (uint32_t)stage_row, stage, (uint32_t)stage_row, rows, (uint32_t)(len >> 4),
+            gtid);
+      else
+        for (uint32_t i = gwarp; i < rows; i += 4)
+          symm::warp_copy<SYMM_PC_UNROLL, symm::kCG, symm::kCS>(dst + i * stage_row,
+                                                                 stage + i * stage_row, len, lane);
     }
     symm::group_sync(bar_id, kPcGroup);  // the group's copies precede the release
     if (gtid == 0) {
@@ -578,6 +623,10 @@ static int combine_pc(symm_heap* h, size_t in_off, size_t out_off, size_t nbytes
   a.budget_ns = h->spin_budget;
   a.ctl = reinterpret_cast<Control*>(h->base);
   a.heap_base = h->base;
+  // stage_row = H*W*D*es is the widest row stride of a tile
+  const bool flat = ((size_t)D * es) % 16 == 0 && ((size_t)bd * es) % 16 == 0 &&
+                    in_off % 16 == 0 && out_off % 16 == 0 && st_off % 16 == 0 &&
+                    (uint64_t)tile_s * H * W * D * es < (1ull << 32);
   // tasks of one S block, dealt evenly: k per CTA, ceil(tasks / k) CTAs, never
   // more CTAs than are resident at once
   const size_t tasks = (size_t)W * W * H * nbd;
@@ -587,18 +636,21 @@ static int combine_pc(symm_heap* h, size_t in_off, size_t out_off, size_t nbytes
   const bool prefetch = !(flags & SYMM_A2A_FLAG_VECTOR) && ((size_t)D * es) % 16 == 0 &&
                         ((size_t)bd * es) % 16 == 0 && in_off % 16 == 0 &&
                         tile_bytes <= kPcMaxPrefetchTile;
-  const void* kfn = prefetch ? (const void*)a2a_pc_kernel<true> : (const void*)a2a_pc_kernel<false>;
+  const void* kfn = prefetch ? (flat ? (const void*)a2a_pc_kernel<true, true>
+                                     : (const void*)a2a_pc_kernel<true, false>)
+                            : (flat ? (const void*)a2a_pc_kernel<false, true>
+                                    : (const void*)a2a_pc_kernel<false, false>);
   const size_t smem = prefetch ? 128 + (size_t)kPcPrefetch * tile_bytes : 0;
   const int cap = resident_ctas(kfn, kPcThreads, smem,
                                 prefetch ? 128 + (size_t)kPcPrefetch * kPcMaxPrefetchTile : 0);
   if (cap <= 0) return fail(SYMM_ECUDA, "all2all_combine: occupancy query failed");
   const size_t per_cta = (tasks + cap - 1) / cap;
   const int grid = (int)((tasks + per_cta - 1) / per_cta);
-  if (prefetch)
-    a2a_pc_kernel<true><<<grid, kPcThreads, smem, s>>>(a, (uint32_t)tile_bytes);
-  else
-    a2a_pc_kernel<false><<<grid, kPcThreads, 0, s>>>(a, 0u);
-  return cuda_check(cudaGetLastError(), "all2all_combine: PC launch");
+  void* args[] = {&a, nullptr};
+  uint32_t tb = prefetch ? (uint32_t)tile_bytes : 0u;
+  args[1] = &tb;
+  return cuda_check(cudaLaunchKernel(kfn, dim3((unsigned)grid), dim3(kPcThreads), args, smem, s),
+                    "all2all_combine: PC launch");
 }
 
 extern "C" int all2all_combine(symm_heap_t* h, const void* in, void* out, int W, int S, int H,
