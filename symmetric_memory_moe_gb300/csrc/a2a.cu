@@ -215,33 +215,6 @@ struct PcArgs {
   const uint8_t* heap_base;
 };
 
-// One tile (rows x vrow 16-byte vectors, rows dst_row / src_row bytes apart)
-// copied by a 128-thread group with the tile flattened to vectors, so narrow
-// rows still keep every thread busy; U vectors in flight per thread.  Offsets
-// inside the tile are 32-bit (the host allows this copy only for tiles whose
-// rows span less than 4 GiB).
-template <int U, symm::LoadKind LK, symm::StoreKind SK>
-__device__ __forceinline__ void group_copy_tile(uint8_t* dst, uint32_t dst_row,
-                                                const uint8_t* src, uint32_t src_row,
-                                                uint32_t rows, uint32_t vrow, int gtid) {
-  const uint32_t nv = rows * vrow;
-  for (uint32_t v0 = gtid; v0 < nv; v0 += kPcGroup * U) {
-    uint4 x[U];
-    uint32_t off_s[U], off_d[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint32_t v = v0 + u * kPcGroup;
-      const uint32_t i = v / vrow, c = v - i * vrow;
-      off_s[u] = i * src_row + 16 * c;
-      off_d[u] = i * dst_row + 16 * c;
-      if (v < nv) x[u] = symm::ld16<LK>(src + off_s[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (v0 + u * kPcGroup < nv) symm::st16k<SK>(dst + off_d[u], x[u]);
-  }
-}
-
 // Input rows of one producer task (tile of S block b, slot q), for the
 // bulk prefetch: q = blockIdx.x + j*gridDim.x is the CTA's j-th slot.
 struct PcTile {
@@ -286,9 +259,13 @@ __device__ __forceinline__ void pc_prefetch(const PcArgs& a, uint32_t nq, uint64
 #endif
 constexpr int kPcPrefetch = SYMM_PC_PREFETCH;
 constexpr uint32_t kPcMaxPrefetchTile = 32 * 1024;
+// Narrowest tile row worth a bulk copy: measured on GB300, rows of 256 B to
+// 1 KB went faster without the prefetch (e.g. 1425 against 936 GB/s on 256 B
+// rows), rows of 2 KB faster with it (4742 against 4302 GB/s).
+constexpr size_t kPcMinPrefetchRow = 2048;
 
 // FLAT: every tile row, base and row stride is 16-byte aligned and a tile
-// spans less than 4 GiB, so whole tiles are copied by group_copy_tile;
+// spans less than 4 GiB, so whole tiles are copied by symm::group_copy_tile;
 // otherwise row by row with warp_copy (any alignment).
 template <bool PREFETCH, bool FLAT>
 __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
@@ -381,7 +358,7 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
             a.in + r * a.slab + (((size_t)(d * a.S + s0) * a.H + h) * a.D + x0) * a.es;
         const size_t src_row = (size_t)a.H * a.D * a.es;
         if (FLAT)
-          group_copy_tile<SYMM_PC_FLAT_UNROLL, symm::kRO, symm::kST>(
+          symm::group_copy_tile<kPcGroup, SYMM_PC_FLAT_UNROLL, symm::kRO, symm::kST>(
               stage, (uint32_t)stage_row, src, (uint32_t)src_row, rows, (uint32_t)(len >> 4),
               gtid);
         else
@@ -393,7 +370,7 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
       // consumer: staged tile -> output rows s0 + i, column r*H + h
       uint8_t* dst = a.out + d * a.slab + ((size_t)s0 * a.H * a.W * a.D) * a.es + stage_col;
       if (FLAT)
-        group_copy_tile<SYMM_PC_FLAT_UNROLL, symm::kCG, symm::kCS>(
+        symm::group_copy_tile<kPcGroup, SYMM_PC_FLAT_UNROLL, symm::kCG, symm::kCS>(
             dst, (uint32_t)stage_row, stage, (uint32_t)stage_row, rows, (uint32_t)(len >> 4),
             gtid);
       else
@@ -630,12 +607,13 @@ static int combine_pc(symm_heap* h, size_t in_off, size_t out_off, size_t nbytes
   // tasks of one S block, dealt evenly: k per CTA, ceil(tasks / k) CTAs, never
   // more CTAs than are resident at once
   const size_t tasks = (size_t)W * W * H * nbd;
-  // input prefetch by bulk copies when every tile row is 16-byte aligned and a
-  // tile fits the shared-memory ring
+  // input prefetch by bulk copies (one per tile row) when every tile row is
+  // 16-byte aligned and at least kPcMinPrefetchRow bytes, and a tile fits the
+  // shared-memory ring; narrower rows are copied faster by the group itself
   const size_t tile_bytes = (size_t)tile_s * bd * es;
   const bool prefetch = !(flags & SYMM_A2A_FLAG_VECTOR) && ((size_t)D * es) % 16 == 0 &&
                         ((size_t)bd * es) % 16 == 0 && in_off % 16 == 0 &&
-                        tile_bytes <= kPcMaxPrefetchTile;
+                        (size_t)bd * es >= kPcMinPrefetchRow && tile_bytes <= kPcMaxPrefetchTile;
   const void* kfn = prefetch ? (flat ? (const void*)a2a_pc_kernel<true, true>
                                      : (const void*)a2a_pc_kernel<true, false>)
                             : (flat ? (const void*)a2a_pc_kernel<false, true>

@@ -62,7 +62,10 @@ __global__ void noalloc_signal_reset_kernel(uint8_t* signals, size_t stride, uin
 // Same task loop as the heap-workspace kernel: a CTA owns fixed (d, r, h,
 // D-block) slots for every S block; its producer warps stage a tile and
 // release the slot, its consumer warps acquire it, copy the tile out and
-// release it back to 0.
+// release it back to 0.  FLAT: tile rows, bases and row strides are 16-byte
+// aligned and a tile spans less than 4 GiB, so each group copies whole tiles
+// flattened to 16-byte vectors; otherwise row by row with warp_copy.
+template <bool FLAT>
 __global__ void __launch_bounds__(kThreads, 3) a2a_pc_noalloc_kernel(const NoallocArgs a) {
   __shared__ int status[2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -104,14 +107,24 @@ __global__ void __launch_bounds__(kThreads, 3) a2a_pc_noalloc_kernel(const Noall
         const uint8_t* src =
             a.in + r * a.slab + (((size_t)(d * a.S + s0) * a.H + h) * a.D + x0) * a.es;
         const size_t src_row = (size_t)a.H * a.D * a.es;
-        for (uint32_t i = gwarp; i < rows; i += 4)
-          symm::warp_copy<4, symm::kRO, symm::kST>(stage + i * stage_row, src + i * src_row, len,
-                                                    lane);
+        if (FLAT)
+          symm::group_copy_tile<kGroup, 4, symm::kRO, symm::kST>(
+              stage, (uint32_t)stage_row, src, (uint32_t)src_row, rows, (uint32_t)(len >> 4),
+              gtid);
+        else
+          for (uint32_t i = gwarp; i < rows; i += 4)
+            symm::warp_copy<4, symm::kRO, symm::kST>(stage + i * stage_row, src + i * src_row,
+                                                      len, lane);
       } else {
         uint8_t* dst = a.out + d * a.slab + ((size_t)s0 * a.H * a.W * a.D) * a.es + stage_col;
-        for (uint32_t i = gwarp; i < rows; i += 4)
-          symm::warp_copy<4, symm::kCG, symm::kCS>(dst + i * stage_row, stage + i * stage_row,
-                                                    len, lane);
+        if (FLAT)
+          symm::group_copy_tile<kGroup, 4, symm::kCG, symm::kCS>(
+              dst, (uint32_t)stage_row, stage, (uint32_t)stage_row, rows, (uint32_t)(len >> 4),
+              gtid);
+        else
+          for (uint32_t i = gwarp; i < rows; i += 4)
+            symm::warp_copy<4, symm::kCG, symm::kCS>(dst + i * stage_row, stage + i * stage_row,
+                                                      len, lane);
       }
       symm::group_sync(bar_id, kGroup);
       if (gtid == 0) symm::st_release(slot, role == 0 ? 1 : 0);
@@ -148,8 +161,9 @@ int resident(int threads) {
   auto it = cache.find(dev);
   if (it != cache.end()) return it->second;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, a2a_pc_noalloc_kernel, threads, 0) !=
-      cudaSuccess)
+  // both instances have the same launch bounds (256 threads, 3 CTAs per SM)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, a2a_pc_noalloc_kernel<false>, threads,
+                                                    0) != cudaSuccess)
     return 0;
   return cache[dev] = per_sm * sm_count();
 }
@@ -238,6 +252,12 @@ extern "C" int all2all_combine_pc_noalloc(symm_heap_t* h, const void* in, void* 
   if (cap <= 0) return fail(SYMM_ECUDA, std::string(what) + ": occupancy query failed");
   const size_t per_cta = (tasks + cap - 1) / cap;
   const int grid = (int)((tasks + per_cta - 1) / per_cta);
-  a2a_pc_noalloc_kernel<<<grid, kThreads, 0, s>>>(a);
+  const bool flat = ((size_t)D * elem_bytes) % 16 == 0 && ((size_t)bd * elem_bytes) % 16 == 0 &&
+                    in_off % 16 == 0 && out_off % 16 == 0 &&
+                    (uint64_t)tile_s * H * W * D * elem_bytes < (1ull << 32);
+  if (flat)
+    a2a_pc_noalloc_kernel<true><<<grid, kThreads, 0, s>>>(a);
+  else
+    a2a_pc_noalloc_kernel<false><<<grid, kThreads, 0, s>>>(a);
   return cuda_check(cudaGetLastError(), "all2all_combine_pc_noalloc: launch");
 }

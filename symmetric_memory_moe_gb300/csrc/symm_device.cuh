@@ -210,6 +210,32 @@ __device__ __forceinline__ void warp_copy_aligned(uint8_t* dst, const uint8_t* s
     if (j + 32 * u < nvec) st16k<SK>(dst + 16 * (j + 32 * u), v[u]);
 }
 
+// One tile (rows x vrow 16-byte vectors, rows dst_row / src_row bytes apart)
+// copied by a group of G threads (gtid = 0 .. G-1) with the tile flattened
+// to vectors, so narrow rows still keep every thread busy; U vectors in
+// flight per thread.  Offsets inside the tile are 32-bit: the caller keeps
+// rows * max(dst_row, src_row) below 4 GiB.
+template <int G, int U, int LK, int SK>
+__device__ __forceinline__ void group_copy_tile(uint8_t* dst, uint32_t dst_row,
+                                                const uint8_t* src, uint32_t src_row,
+                                                uint32_t rows, uint32_t vrow, int gtid) {
+  const uint32_t nv = rows * vrow;
+  for (uint32_t v0 = gtid; v0 < nv; v0 += G * U) {
+    uint4 x[U];
+    uint32_t off_d[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t v = v0 + u * G;
+      const uint32_t i = v / vrow, c = v - i * vrow;
+      off_d[u] = i * dst_row + 16 * c;
+      if (v < nv) x[u] = ld16<LK>(src + (i * src_row + 16 * c));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (v0 + u * G < nv) st16k<SK>(dst + off_d[u], x[u]);
+  }
+}
+
 // Bytes m..m+15 (1 <= m <= 15) of the 32-byte little-endian concatenation a|b.
 __device__ __forceinline__ uint4 funnel16(uint4 a, uint4 b, unsigned m) {
   uint64_t w0 = (uint64_t)a.x | ((uint64_t)a.y << 32);

@@ -192,7 +192,7 @@ def test_unaligned_base_pointers(in_shift, out_shift, variant):
 
 
 @pytest.mark.parametrize("in_shift,out_shift,tile_s", [
-    (0, 0, 8),      # 16-byte-aligned tiles: bulk prefetch, whole-tile group copies
+    (0, 0, 8),      # 16-byte-aligned 16 KB tiles: bulk prefetch, whole-tile group copies
     (0, 8, 8),      # output off 16 bytes: bulk prefetch, row-by-row copies
     (4, 0, 8),      # input off 16 bytes: no prefetch, row-by-row copies
     (0, 0, 40),     # a tile too big for the prefetch ring: whole-tile group copies
@@ -200,10 +200,11 @@ def test_unaligned_base_pointers(in_shift, out_shift, variant):
 ])
 def test_pc_copy_instances(in_shift, out_shift, tile_s):
     """The producer/consumer kernel's four copy instances, chosen by alignment
-    and tile size, on 976-byte rows and a ragged last S block (40-row tiles
-    are 38 KB, more than the prefetch ring takes).  Each object leaves 128
-    bytes of its 256-byte allocation granule free for the shifts."""
-    W, S, H, D, es = 4, 45, 2, 488, 2
+    and tile size, on 2064-byte rows (wide enough for the bulk prefetch) and
+    a ragged last S block (40-row tiles are 81 KB, more than the prefetch
+    ring takes).  Each object leaves 128 bytes of its 256-byte allocation
+    granule free for the shifts."""
+    W, S, H, D, es = 4, 45, 2, 1032, 2
     xe = _rand_bytes(W, S * W, H, D, es, seed=tile_s + in_shift).reshape(W, S * W, H, D, es)
     got = _run_es(xe, W, S, H, D, es, "pc", tile_s, 0, 2, in_shift, out_shift)
     assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
