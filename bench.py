@@ -3,20 +3,30 @@
 One step = one all2all_combine through the C ABI over W=8 emulated PEs
 (per PE (16384, 1, 7168) bf16 -> (2048, 8, 7168)): T = 1.879 GB read and
 1.879 GB written.  GB/s = 2*T / step time.  The input (1.88 GB) is larger
-than L2, so no flush is needed between steps.
+than L2, so no flush is needed between steps.  After the timed steps the
+other configurations' headline variants are timed in the same process and
+reported under `variants`.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--variant pc|direct]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--variant direct|pc]
   python bench.py --impl reference ...   # the CPU oracle as the reference arm
 
-For N > 1 (torchrun), every rank runs its own replica on its own GPU (the
-W PEs are emulated inside one GPU; there is no cross-GPU exchange), the step
-time is the max over ranks and the value the sum of all ranks' bytes over it.
+Ranks: under torchrun (WORLD_SIZE set) this process is one rank.  Otherwise
+`--gpus N` with N > 1 starts N processes itself, one per GPU (RANK,
+LOCAL_RANK, WORLD_SIZE, MASTER_ADDR=127.0.0.1 and a free MASTER_PORT in
+their environment).  Every rank runs its own replica on its own GPU (the W
+PEs are emulated inside one GPU; there is no cross-GPU exchange); the
+process group carries only the barrier and the max of the step times, and
+the value is all ranks' bytes over that max.  `--dry-run` runs the same
+orchestration without a GPU (gloo, a host-side stand-in step) so that the
+launcher can be checked on CPU; it prints no benchmark figure.
 """
 from __future__ import annotations
 
 import argparse
 import json
 import os
+import platform
+import socket
 import statistics
 import subprocess
 import sys
@@ -32,6 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = "dsv3"
 PC_TILE_S, PC_BLOCK_D, PC_BUFFERS = 16, 1024, 2
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+L2_BYTES = 126 * 2**20  # smaller than the part's L2: data this size stays resident
 
 
 def _hbm_peak():
@@ -40,6 +51,16 @@ def _hbm_peak():
             return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def bench_config(world: int, variant: str) -> dict:
+    """The workload as both arms report it."""
+    return {"workload": "combine DeepSeek-V3-shaped: W=8 emulated PEs, per PE "
+                        "(16384,1,7168) bf16 -> (2048,8,7168)",
+            "W": 8, "S": 2048, "H": 1, "D": 7168, "dtype": "bf16", "variant": variant,
+            "bytes_per_step": 2 * 8 * 16384 * 7168 * 2, "parallelism": f"replicas{world}",
+            "l2": "no flush: 1.88 GB input and output per step, >> 126 MB L2",
+            "pc_tile_s": PC_TILE_S, "pc_block_d": PC_BLOCK_D, "pc_buffer_num": PC_BUFFERS}
 
 
 def _kernel_sources_hash(files) -> str:
@@ -56,16 +77,21 @@ def _kernel_sources_hash(files) -> str:
 
 
 def _traffic(kernel: str, launch_bytes: int):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel
-    sources are unchanged since it was taken (else None)."""
+    """DRAM bytes of a launch moving `launch_bytes` algorithmic bytes, from the
+    committed ncu captures, while the kernel sources still hash to the
+    captured ones (else None).  Two captures of different sizes give the
+    DRAM bytes per algorithmic byte as their slope: a launch that leaves dirty
+    lines in L2 at its end writes them back during the next one, so the
+    per-launch traffic of a long run of launches is the slope times the
+    launch's bytes, not one capture scaled."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
         e = t["kernels"][kernel]
         if e.get("sources_hash") != _kernel_sources_hash(e["sources"]):
             return None
-        # scaled from the captured launch by the bytes one launch moves
-        return int(round(e["dram_bytes"] * launch_bytes / e["algorithmic_bytes"]))
+        (a0, d0), (a1, d1) = [(c["algorithmic_bytes"], c["dram_bytes"]) for c in e["captures"]]
+        return int(round((d1 - d0) / (a1 - a0) * launch_bytes))
     except Exception:
         return None
 
@@ -159,21 +185,97 @@ def barrier(device=None):
             dist.barrier()
 
 
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch(args, argv) -> int:
+    """Runs this script as args.gpus ranks (one process each, rank r on GPU r)
+    and returns the first non-zero exit code, else 0.  Rank 0 prints the
+    line; the ranks inherit this process's stdout and stderr."""
+    port = _free_port()
+    procs = []
+    for r in range(args.gpus):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(args.gpus),
+                   LOCAL_WORLD_SIZE=str(args.gpus), MASTER_ADDR="127.0.0.1",
+                   MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__)] + argv,
+                                      env=env))
+    codes = [p.wait() for p in procs]
+    return next((c for c in codes if c), 0)
+
+
+def _init_group(backend: str, device=None):
+    import torch.distributed as dist
+
+    world, _, _ = _dist_env()
+    if world > 1 and not dist.is_initialized():
+        if device is not None:
+            dist.init_process_group(backend, device_id=device)
+        else:
+            dist.init_process_group(backend)
+
+
+def run_dry(args):
+    """The launcher and rank plumbing without a GPU: gloo, a host-side
+    stand-in step, the same barrier / max-over-ranks / rank-0 line.  Prints
+    no benchmark figure."""
+    import torch.distributed as dist
+
+    world, rank, local = _dist_env()
+    _init_group("gloo")
+    buf = bytearray(1 << 20)
+    for _ in range(args.warmup):
+        bytes(buf)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        bytes(buf)
+    t = max_over_ranks(time.perf_counter() - t0)
+    reports = [None] * world
+    if world > 1:
+        dist.all_gather_object(reports, {"rank": rank, "local_rank": local})
+    else:
+        reports = [{"rank": rank, "local_rank": local}]
+    if rank == 0:
+        print(json.dumps({"dry_run": True, "metric": METRIC, "value": None, "unit": UNIT,
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ranks_reported": sorted(r["rank"] for r in reports),
+                          "local_ranks": sorted(r["local_rank"] for r in reports),
+                          "max_host_step_s": t / max(1, args.steps)}), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 # --------------------------------------------------------------- oracle ---
-def oracle_rate(wl, rows: int, repeats_min_s: float, max_runs: int = 50):
-    """The CPU oracle (as it stands, one thread) on the workload's shape with
-    `rows` rows per (source, destination) block; returns (GB/s, seconds per
-    run, runs, sample bytes moved per run)."""
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def _oracle_sample(wl, rows: int):
     import torch
 
-    import oracle
     from symmetric_memory_moe_gb300 import inputs
 
-    o = oracle.load()
     sample = inputs.Workload(wl.name, "combine", wl.W, rows, wl.H, wl.D, wl.dtype, wl.dist,
                              wl.seed)
     x = inputs.make_input(sample)
-    xb = (x.view(torch.int16) if x.dtype == torch.bfloat16 else x).numpy()
+    return (x.view(torch.int16) if x.dtype == torch.bfloat16 else x).numpy()
+
+
+def oracle_rate(o, xb, wl, rows: int, min_s: float, max_runs: int = 50):
+    """Times the oracle `o` on a token sample `xb` of the workload (`rows` rows
+    per (source, destination) block); returns (GB/s, median s per run, runs,
+    bytes moved per run)."""
     moved = 2 * xb.nbytes
     times = []
     t_start = time.perf_counter()
@@ -181,10 +283,40 @@ def oracle_rate(wl, rows: int, repeats_min_s: float, max_runs: int = 50):
         t0 = time.perf_counter()
         o.combine(xb, wl.W, rows, wl.H, wl.D)
         times.append(time.perf_counter() - t0)
-        if time.perf_counter() - t_start >= repeats_min_s and len(times) >= 1:
+        if time.perf_counter() - t_start >= min_s:
             break
     med = statistics.median(times)
     return moved / med / 1e9, med, len(times), moved
+
+
+def cpu_baseline(wl, min_s: float = 8.0) -> dict:
+    """The oracle on the machine's host cores: its OpenMP build (the combine's loop
+    over the W destinations split across threads) and the plain build on one
+    thread, each on a token sample for about min_s seconds."""
+    import oracle
+
+    nproc = os.cpu_count() or 1
+    threads = min(nproc, wl.W)  # the parallel loop has W iterations
+    rows = 512
+    xb = _oracle_sample(wl, rows)
+    one, sec1, runs1, moved = oracle_rate(oracle.load(), xb, wl, rows, min_s)
+    line = {"value": round(one, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"oracle combine on W={wl.W} S={rows} H={wl.H} D={wl.D} bf16 ({rows}/"
+                      f"{wl.S} of the tokens, {moved / 1e9:.3f} GB moved), median of {runs1} "
+                      f"runs ({sec1:.2f} s each), one thread",
+            "nproc": nproc, "cpu_model": _cpu_model()}
+    try:
+        os.environ["OMP_NUM_THREADS"] = str(threads)
+        many, secn, runsn, _ = oracle_rate(oracle.load_openmp(), xb, wl, rows, min_s)
+    except Exception as e:  # no OpenMP runtime on this host
+        line["parallel_unavailable"] = str(e)[:200]
+        return line
+    line.update({"value": round(many, 4), "cores": threads,
+                 "sample": line["sample"].replace("one thread", "") +
+                 f"; OpenMP build over the {wl.W} destinations on {threads} threads: "
+                 f"median of {runsn} runs ({secn:.2f} s each)",
+                 "single_thread": {"value": round(one, 4), "unit": UNIT, "cores": 1}})
+    return line
 
 
 def run_reference(args):
@@ -192,45 +324,202 @@ def run_reference(args):
     world, rank, _ = _dist_env()
     if rank != 0:
         return
+    import oracle
     from symmetric_memory_moe_gb300 import inputs
 
     wl = inputs.WORKLOADS[WORKLOAD]
-    # size each step so warm-up + steps end within ~2 minutes
-    rate, _, _, _ = oracle_rate(wl, 8, 0.0, max_runs=1)
+    nproc = os.cpu_count() or 1
+    threads = min(nproc, wl.W)
+    os.environ["OMP_NUM_THREADS"] = str(threads)
+    try:
+        o, kind = oracle.load_openmp(), f"OpenMP build over the {wl.W} destinations, " \
+                                        f"{threads} threads"
+    except Exception:
+        o, kind, threads = oracle.load(), "plain build, one thread", 1
+    # size each step so that warm-up + steps end within about two minutes
+    probe = _oracle_sample(wl, 8)
+    rate, _, _, _ = oracle_rate(o, probe, wl, 8, 0.0, max_runs=1)
     per_row = 2 * wl.W * wl.W * wl.H * wl.D * wl.es
     budget = 120.0 / max(1, args.steps + args.warmup)
     rows = int(max(1, min(wl.S, budget * rate * 1e9 / per_row)))
-    sample_rate, sec, _, moved = 0.0, 0.0, 0, rows * per_row
-    import oracle
-    import torch
-
-    o = oracle.load()
-    sample = inputs.Workload(wl.name, "combine", wl.W, rows, wl.H, wl.D, wl.dtype, wl.dist,
-                             wl.seed)
-    xb = inputs.make_input(sample).view(torch.int16).numpy()
+    xb = _oracle_sample(wl, rows)
+    moved = rows * per_row
     for _ in range(args.warmup):
         o.combine(xb, wl.W, rows, wl.H, wl.D)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         o.combine(xb, wl.W, rows, wl.H, wl.D)
     sec = (time.perf_counter() - t0) / max(1, args.steps)
-    sample_rate = moved / sec / 1e9
+    value = round(moved / sec / 1e9, 4)
     desc = (f"oracle combine on W={wl.W} S={rows} H={wl.H} D={wl.D} bf16 "
-            f"({rows}/{wl.S} of the tokens), {moved / 1e9:.3f} GB moved per step")
+            f"({rows}/{wl.S} of the tokens), {moved / 1e9:.3f} GB moved per step; {kind}")
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(sample_rate, 4), "unit": UNIT,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
-        "config": {"workload": "combine DeepSeek-V3-shaped (W=8 S=2048 H=1 D=7168 bf16), "
-                               "CPU oracle on a token sample", "W": wl.W, "S_sample": rows,
-                   "H": wl.H, "D": wl.D},
-        "cpu_baseline": {"value": round(sample_rate, 4), "unit": UNIT, "cores": 1,
-                         "kind": "oracle", "sample": desc},
-        "e2e": {"value": round(sample_rate, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
+        "config": bench_config(world, args.variant),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc, "nproc": nproc, "cpu_model": _cpu_model()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ variants ---
+def _fill_random(heap, ptr, nbytes, seed):
+    """Seeded random bytes in every PE's copy of an object (the path moves
+    raw bits, so bytes stand in for the workload's values when timing)."""
+    import torch
+
+    g = torch.Generator(device=heap.mem.device).manual_seed(seed)
+    heap.views(ptr, nbytes).copy_(torch.randint(0, 256, (heap.npes, nbytes), generator=g,
+                                                dtype=torch.uint8, device=heap.mem.device))
+
+
+def _time_calls(call, steps, warmup, graph):
+    """GPU ms per call: `steps` launches timed with CUDA events, or, for
+    calls whose data stay in L2 (launch-bound from Python), `steps` replays
+    of a CUDA graph of 20 calls."""
+    import torch
+
+    for _ in range(max(3, warmup)):
+        call()
+    torch.cuda.synchronize()
+    if graph:
+        per_graph = 20
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(per_graph):
+                    call()
+        torch.cuda.current_stream().wait_stream(s)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (steps * per_graph)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def _check_runs(heap, inp, out, W, S, run, inverse=False, samples=16, seed=0):
+    """Sampled runs of the permutation: out_d[s, r] == in_r[d*S + s] (combine,
+    dispatch with S per block), or its inverse."""
+    import torch
+
+    n = W * S * run
+    outv = heap.views(out, n).view(W, S if not inverse else W, W if not inverse else S, run)
+    inv = heap.views(inp, n).view(W, W if not inverse else S, S if not inverse else W, run)
+    g = torch.Generator().manual_seed(seed)
+    for _ in range(samples):
+        d, s, r = (int(torch.randint(0, k, (1,), generator=g)) for k in (W, S, W))
+        if not inverse:
+            ok = torch.equal(outv[d, s, r], inv[r, d, s])   # out_d[s, r] = in_r[d*S + s]
+        else:
+            ok = torch.equal(outv[r, d, s], inv[d, s, r])   # out_r[d*S + s] = in_d[s, r]
+        if not ok:
+            raise RuntimeError("a timed variant produced a wrong output run")
+
+
+def time_variants(args, peak):
+    """The other configurations' headline variants (and the two-phase
+    combine on the DeepSeek-V3 shape), each timed in this process."""
+    from symmetric_memory_moe_gb300 import abi
+    from symmetric_memory_moe_gb300.torch_heap import CombineBuffers, TorchSymmHeap
+
+    out = {}
+
+    def done(heap):
+        rc, info = abi.symm_check_error(heap.handle)
+        heap.close()
+        if rc != abi.SYMM_OK:
+            raise RuntimeError(f"a timed variant's device wait gave up (info {info})")
+
+    def record(name, workload, bytes_step, ms, timing, extra=None):
+        gbs = bytes_step / (ms * 1e-3) / 1e9
+        e = {"workload": workload, "gbs": round(gbs, 1), "ms_per_step": round(ms, 5),
+             "frac_of_peak": round(gbs / peak, 4), "bytes_per_step": bytes_step,
+             "l2_resident": bytes_step <= L2_BYTES, "timing": timing}
+        e.update(extra or {})
+        out[name] = e
+
+    steps = max(args.steps, 10)
+    # small: W8 S128 H8 D128 bf16 (16.8 MB in, L2-resident), direct and P/C
+    W, S, H, D, es = 8, 128, 8, 128, 2
+    for variant, tile in (("direct", 0), ("pc", 64)):
+        b = CombineBuffers(W, S * W, H, D, es, pc=variant == "pc", S=S, tile_s=tile or 16)
+        _fill_random(b.heap, b.inp, b.nbytes, 1)
+        kind = abi.SYMM_A2A_PC if variant == "pc" else abi.SYMM_A2A_DIRECT
+
+        def call(b=b, kind=kind, tile=tile):
+            abi.all2all_combine(b.heap.handle, b.inp, b.out, W, S, H, D, es, kind, tile or 16, 0,
+                                2, b.staging, b.signals)
+        ms = _time_calls(call, steps, args.warmup, graph=True)
+        _check_runs(b.heap, b.inp, b.out, W, S, H * D * es)
+        record(f"small_{variant}", "combine small: W=8 S=128 H=8 D=128 bf16", 2 * W * b.nbytes,
+               ms, "CUDA graph of 20 calls", {"tile_s": tile} if tile else None)
+        done(b.heap)
+    # round trip: W16 S1024 H4 D128 fp16, dispatch then its inverse
+    W, S, H, D, es = 16, 1024, 4, 128, 2
+    n = S * H * D * es
+    heap = TorchSymmHeap(W, 3 * n + (4 << 20))
+    x, y, z = heap.malloc(n), heap.malloc(n), heap.malloc(n)
+    _fill_random(heap, x, n, 3)
+    ms = _time_calls(lambda: abi.all2all_dispatch(heap.handle, x, y, W, S, H, D, es), steps,
+                     args.warmup, graph=True)
+    _check_runs(heap, x, y, W, S // W, H * D * es)
+    record("roundtrip_dispatch", "dispatch: W=16 S=1024 H=4 D=128 fp16", 2 * W * n, ms,
+           "CUDA graph of 20 calls")
+    ms = _time_calls(lambda: abi.all2all_combine_back(heap.handle, y, z, W, S // W, H, D, es),
+                     steps, args.warmup, graph=True)
+    if not heap.views(z, n).equal(heap.views(x, n)):
+        raise RuntimeError("dispatch then its inverse did not round-trip")
+    record("roundtrip_combine_back", "combine back: W=16 S'=64 H=4 D=128 fp16", 2 * W * n, ms,
+           "CUDA graph of 20 calls")
+    done(heap)
+    # tail: W32 S256 H2 D999 fp16 (1998-byte rows), direct and P/C with 32-row tiles
+    W, S, H, D, es = 32, 256, 2, 999, 2
+    for variant in ("direct", "pc"):
+        b = CombineBuffers(W, S * W, H, D, es, pc=variant == "pc", S=S, tile_s=32)
+        _fill_random(b.heap, b.inp, b.nbytes, 4)
+        kind = abi.SYMM_A2A_PC if variant == "pc" else abi.SYMM_A2A_DIRECT
+
+        def call(b=b, kind=kind):
+            abi.all2all_combine(b.heap.handle, b.inp, b.out, W, S, H, D, es, kind, 32, 0, 2,
+                                b.staging, b.signals)
+        ms = _time_calls(call, steps, args.warmup, graph=False)
+        _check_runs(b.heap, b.inp, b.out, W, S, H * D * es)
+        record(f"tail_{variant}", "combine tail: W=32 S=256 H=2 D=999 fp16", 2 * W * b.nbytes,
+               ms, "launches", {"tile_s": 32} if variant == "pc" else None)
+        done(b.heap)
+    # the two-phase combine on the DeepSeek-V3 shape (tiles of 64 x 1024)
+    W, S, H, D, es = 8, 2048, 1, 7168, 2
+    n = S * W * H * D * es
+    nb, ns = abi.all2all_two_phase_workspace(W, S, H, D, es, 64, 1024, 2)
+    heap = TorchSymmHeap(W, 2 * n + nb + ns + (4 << 20))
+    x, y, bulk, sig = heap.malloc(n), heap.malloc(n), heap.malloc(nb), heap.malloc(ns)
+    _fill_random(heap, x, n, 2)
+    ms = _time_calls(lambda: abi.all2all_combine_two_phase(heap.handle, x, y, W, S, H, D, es, 64,
+                                                           1024, 2, bulk, sig),
+                     steps, args.warmup, graph=False)
+    _check_runs(heap, x, y, W, S, H * D * es)
+    record("dsv3_two_phase", "combine DeepSeek-V3-shaped, two-phase", 2 * W * n, ms, "launches",
+           {"tile_s": 64, "block_d": 1024})
+    done(heap)
+    return out
 
 
 # ------------------------------------------------------------------ ours ---
@@ -242,11 +531,10 @@ def run_ours(args):
     from symmetric_memory_moe_gb300.torch_heap import CombineBuffers
 
     world, rank, local = _dist_env()
-    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU (or --dry-run)"
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    if world > 1 and not dist.is_initialized():
-        dist.init_process_group("nccl", device_id=device)
+    _init_group("nccl", device)
 
     wl = inputs.WORKLOADS[WORKLOAD]
     W, S, H, D, es = wl.W, wl.S, wl.H, wl.D, wl.es
@@ -331,6 +619,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), device) / e2e_steps
     assert abi.symm_check_error(heap.handle)[0] == abi.SYMM_OK
+    heap.close()
+    del host_in, host_out
 
     # plain cudaMemcpyAsync device-to-device of the same T bytes, for context
     src = torch.empty(T, dtype=torch.uint8, device=device)
@@ -345,18 +635,22 @@ def run_ours(args):
     torch.cuda.synchronize()
     d2d_gbs = 2 * T * 10 / (c0.elapsed_time(c1) * 1e-3) / 1e9
     del src, dst
+    torch.cuda.empty_cache()
+
+    peak, peak_src = _hbm_peak()
+    variants = {k: {"workload": "combine DeepSeek-V3-shaped", "gbs": round(v["gbs"], 1),
+                    "ms_per_step": round(v["ms_per_step"], 4),
+                    "frac_of_peak": round(v["gbs"] / world / peak, 4),
+                    "bytes_per_step": step_bytes, "l2_resident": False, "timing": "launches"}
+                for k, v in results.items()}
+    if not args.no_variants:
+        variants.update(time_variants(args, peak))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows = 512
-        rate, sec, runs, moved = oracle_rate(wl, rows, 10.0)
-        cpu = {"value": round(rate, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"oracle combine on W={W} S={rows} H={H} D={D} bf16 ({rows}/{S} of "
-                         f"the tokens, {moved / 1e9:.3f} GB moved), median of {runs} runs "
-                         f"({sec:.2f} s each), one host thread"}
+        cpu = cpu_baseline(wl)
 
     head = results[args.variant]
-    peak, peak_src = _hbm_peak()
     kernel_name = "a2a_pc_kernel" if args.variant == "pc" else "a2a_runs_kernel"
     achieved = step_bytes / (head["launch_ms_avg"] * 1e-3) / 1e9
     line = {
@@ -365,20 +659,14 @@ def run_ours(args):
         "ms_per_step": round(head["ms_per_step"], 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, moved as raw bits)",
-        "config": {"workload": "combine DeepSeek-V3-shaped: W=8 emulated PEs, per PE "
-                               "(16384,1,7168) bf16 -> (2048,8,7168)",
-                   "W": W, "S": S, "H": H, "D": D, "variant": args.variant,
-                   "bytes_per_step": step_bytes, "parallelism": f"replicas{world}",
-                   "l2": "no flush: 1.88 GB input and output per step, >> 126 MB L2",
-                   "pc_tile_s": PC_TILE_S, "pc_block_d": PC_BLOCK_D,
-                   "pc_buffer_num": PC_BUFFERS},
+        "config": bench_config(world, args.variant),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": UNIT,
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "kernel": kernel_name,
-                     "traffic": _traffic(kernel_name, step_bytes)},
-        "variants": {k: {"gbs": round(v["gbs"], 1), "ms_per_step": round(v["ms_per_step"], 4),
-                         "frac_of_peak": round(v["gbs"] / world / peak, 4)}
-                     for k, v in results.items()},
+                     "traffic": _traffic(kernel_name, step_bytes),
+                     "traffic_method": "ncu DRAM bytes of two captures (S=256, S=512): their "
+                                       "slope per algorithmic byte times this launch's bytes"},
+        "variants": variants,
         "d2d_memcpy_gbs": round(d2d_gbs, 1),
         "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": T, "d2h_bytes_per_step": T, "steps": e2e_steps,
@@ -390,26 +678,35 @@ def run_ours(args):
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    heap.close()
     if world > 1 and dist.is_initialized():
         dist.destroy_process_group()
 
 
-def main():
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--variant", default="direct", choices=["direct", "pc"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
+    ap.add_argument("--no-variants", action="store_true",
+                    help="time only the DeepSeek-V3-shaped combine")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="the launcher and rank plumbing on CPU (gloo); no benchmark figure")
+    args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return launch(args, argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.dry_run:
+        run_dry(args)
     else:
         run_ours(args)
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -85,8 +85,12 @@ typedef struct symm_heap symm_heap_t;
  * slab_stride bytes per PE; a multiple of 256 (2 MiB recommended) and
  *             > SYMM_HEAP_HEADER_BYTES.  PE k's slab starts at base + k*slab_stride.
  * npes        number of PEs (W), >= 1.
- * heap        out: host handle.  Touches no device memory (the header is
+ * heap        out: host handle.  Writes no device memory (the header is
  *             zeroed on the stream of the first call that launches work).
+ *             With a current CUDA device, it looks up the address of
+ *             all2all_combine_pc_noalloc's static array on that device (see
+ *             there), which makes CUDA load and reserve that array; a
+ *             failure there is not reported here (the entry point reports it).
  * Errors: SYMM_EINVAL. */
 int symm_heap_init(void *base, size_t slab_stride, int npes, symm_heap_t **heap);
 
@@ -112,14 +116,19 @@ void *symm_at(symm_heap_t *heap, const void *ptr, int pe);
 /* Default spin budget of producer/consumer waits, in ns (initially 2 s). */
 int symm_set_spin_budget(symm_heap_t *heap, uint64_t budget_ns);
 
+/* Marks, in the *info of symm_check_error, a timed-out signal slot of
+ * all2all_combine_pc_noalloc: *info = SYMM_INFO_NOALLOC_SIGNAL + the slot's
+ * byte offset in the signal area of that call's static array. */
+#define SYMM_INFO_NOALLOC_SIGNAL (1ll << 62)
+
 /* Synchronises `stream`, then returns the first device-side error recorded in
  * the heap header since the last check (SYMM_OK; SYMM_ETIMEDOUT; SYMM_ERANGE
- * from shmem_alltoall; SYMM_EINVAL from a cluster kernel launched without its
- * cluster shape, which then did nothing) and clears
- * it.  Until it is cleared, every later device wait on this heap gives up at
- * once (the abort flag stays raised), so check after any launch that may
- * have timed out.  *info (optional) receives the byte offset from base of the signal that
- * timed out.  Errors: SYMM_ECUDA. */
+ * from shmem_alltoall) and clears it.  Until it is cleared, every later
+ * device wait on this heap gives up at once (the abort flag stays raised),
+ * so check after any launch that may have timed out.  *info (optional)
+ * receives, for a wait that gave up, the byte offset from base of its
+ * signal, or SYMM_INFO_NOALLOC_SIGNAL + an offset for a signal of
+ * all2all_combine_pc_noalloc (see there).  Errors: SYMM_ECUDA. */
 int symm_check_error(symm_heap_t *heap, void *stream, int64_t *info);
 
 /* Message of the last failed call on this thread ("" if none). */
@@ -368,7 +377,8 @@ int shmem_fused_all_gather_matmul(symm_heap_t *heap, const void *a, const void *
  * all2all_combine(SYMM_A2A_PC) except that the staging ring and the signal
  * slots live in the library's static SYMM_NOALLOC_SCRATCH_BYTES array
  * instead of the caller's heap; the caller passes only the symmetric input
- * and output.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ * and output.  It runs the same kernels as all2all_combine(SYMM_A2A_PC) and
+ * calls no cudaMalloc, cudaFree or other allocating routine.
  *  - Needs W * (roundup256(buffer_num*tile_s*H*W*D*elem_bytes) +
  *    roundup256(buffer_num*W*nbd*H*64)) bytes of scratch; larger requests
  *    return SYMM_EINVAL before launching anything.
@@ -376,11 +386,16 @@ int shmem_fused_all_gather_matmul(symm_heap_t *heap, const void *a, const void *
  *    the last call's contents).  All calls share the one array per device:
  *    calls that overlap on the GPU (other streams, other threads, other
  *    heaps) race and give undefined output; order them on one stream.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make
- *    that first call before any stream capture.
+ *  - The array's device address is looked up (cudaGetSymbolAddress, with the
+ *    device current) and cached once per device.  symm_heap_init does this
+ *    for the device current at init, which also loads the part of the
+ *    library that holds the array: that is when CUDA reserves the array's
+ *    memory, so a device without 32 MiB free fails there, not here.  On any
+ *    other device the first call does the look-up itself; make that call
+ *    before any stream capture.
  * Errors: SYMM_EINVAL, SYMM_ECUDA; a wait that gives up shows in
- * symm_check_error(). */
+ * symm_check_error(), with *info = SYMM_INFO_NOALLOC_SIGNAL + the offset of
+ * the slot in the array's signal area. */
 int all2all_combine_pc_noalloc(symm_heap_t *heap, const void *in, void *out, int W, int S, int H,
                                int D, int elem_bytes, int tile_s, int block_d, int buffer_num,
                                void *stream);

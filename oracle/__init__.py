@@ -3,4 +3,4 @@
 TEST INFRASTRUCTURE, NOT PRODUCT CODE: only tests, the smoke check and the
 benchmark's CPU-baseline leg may import it.  See ``a2a_oracle.c``.
 """
-from .oracle import Oracle, build, load  # noqa: F401
+from .oracle import Oracle, build, load, load_openmp  # noqa: F401

@@ -21,17 +21,21 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "a2a_oracle.c")
 BUILD_DIR = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liba2a_oracle.so")
+# the same source built with -fopenmp: oracle_combine splits its loop over the
+# destination rank d across threads.  Only the timed CPU baseline uses it.
+OMP_LIB_PATH = os.path.join(BUILD_DIR, "liba2a_oracle_omp.so")
 
 
 def build(src: str = SOURCE, out: str = LIB_PATH, force: bool = False,
-          werror: bool = True) -> str:
-    """Compile the oracle with gcc -O2 into a shared library; return its path."""
+          werror: bool = True, openmp: bool = False) -> str:
+    """Compile the oracle with gcc -O2 (and -fopenmp if asked) into a shared
+    library; return its path."""
     if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-Wall"] + (["-Werror"] if werror else [])
-    cmd += ["-shared", "-fPIC", "-o", tmp, src]
+    cmd += (["-fopenmp"] if openmp else []) + ["-shared", "-fPIC", "-o", tmp, src]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -240,6 +244,12 @@ def load(path: str | None = None) -> Oracle:
     if _DEFAULT is None:
         _DEFAULT = Oracle()
     return _DEFAULT
+
+
+def load_openmp() -> Oracle:
+    """The oracle built with -fopenmp (its combine runs over d in parallel,
+    OMP_NUM_THREADS threads), for the timed CPU baseline."""
+    return Oracle(build(out=OMP_LIB_PATH, openmp=True))
 
 
 if __name__ == "__main__":  # pragma: no cover - manual build helper

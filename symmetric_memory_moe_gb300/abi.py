@@ -163,12 +163,11 @@ def symm_set_spin_budget(heap: int, budget_ns: int) -> None:
 
 def symm_check_error(heap: int, stream=None):
     """(code, info): SYMM_OK, SYMM_ETIMEDOUT (info: the timed-out signal's byte
-    offset), SYMM_ERANGE, or SYMM_EINVAL (a cluster kernel launched without its
-    cluster shape; info: the cluster size it saw); raises SymmError only for a
-    failure of the check itself."""
+    offset), or SYMM_ERANGE; raises SymmError only for a failure of the check
+    itself."""
     info = _I64(0)
     rc = lib().symm_check_error(heap, _stream(stream), ctypes.byref(info))
-    if rc not in (SYMM_OK, SYMM_ETIMEDOUT, SYMM_ERANGE, SYMM_EINVAL):
+    if rc not in (SYMM_OK, SYMM_ETIMEDOUT, SYMM_ERANGE):
         _check(rc, "symm_check_error")
     return rc, info.value
 

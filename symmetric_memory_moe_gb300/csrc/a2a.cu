@@ -34,6 +34,7 @@
 //    H*D elements (fixed r, d, s) is copied once, the minimum traffic.
 #include <stdio.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <string>
@@ -65,13 +66,21 @@ namespace {
 #ifndef SYMM_RUNS_GENERAL_MIN_BLOCKS
 #define SYMM_RUNS_GENERAL_MIN_BLOCKS 6
 #endif
+// 16-byte vectors in flight per lane in the row-by-row producer/consumer
+// copies (rows whose staging stride is not a multiple of 16 bytes); 3 is the
+// most that fits the register budget of 3 CTAs per SM without spills
 #ifndef SYMM_PC_UNROLL
-#define SYMM_PC_UNROLL 4
+#define SYMM_PC_UNROLL 3
 #endif
 // 16-byte vectors in flight per thread in the producer/consumer tile copies
 // that spread a whole tile over the group (tiles with 16-byte-aligned rows)
 #ifndef SYMM_PC_FLAT_UNROLL
 #define SYMM_PC_FLAT_UNROLL 4
+#endif
+// 16-byte vectors in flight per thread in the tile copies for rows of any
+// alignment (two aligned source blocks per output vector)
+#ifndef SYMM_PC_ANY_UNROLL
+#define SYMM_PC_ANY_UNROLL 4
 #endif
 #ifndef SYMM_PC_MIN_BLOCKS
 #define SYMM_PC_MIN_BLOCKS 3
@@ -202,52 +211,145 @@ __global__ void __launch_bounds__(32)
 }
 
 // ------------------------------------------------ producer / consumer ---
+// The staging ring and the signal slots of PE k sit at staging + k*stage_pe
+// and signals + k*sig_pe: in the destination slab of the symmetric heap
+// (stride = the slab), or in any other device array laid out per PE.
 struct PcArgs {
-  const uint8_t* in;   // PE 0 copies of the symmetric objects; PE k at +k*slab
+  const uint8_t* in;  // PE 0's input and output; PE k's at +k*slab
   uint8_t* out;
-  uint8_t* staging;
-  uint8_t* signals;
   size_t slab;
+  uint8_t* staging;  // PE 0's staging ring [buffer][tile_s rows][H*W][D]
+  uint8_t* signals;  // PE 0's signal slots, SYMM_SIGNAL_STRIDE_BYTES apart
+  size_t stage_pe, sig_pe;
   uint32_t W, H, S, D, es;
   uint32_t tile_s, block_d, nbd, nbs, buffer_num;
+  size_t tile_src;   // input bytes from one S block to the next (tile_s rows)
+  size_t tile_dst;   // output bytes from one S block to the next
+  size_t stage_buf;  // staging bytes from one buffer to the next
+  size_t slot_buf;   // signal bytes from one buffer to the next
   uint64_t budget_ns;
   Control* ctl;
-  const uint8_t* heap_base;
+  const uint8_t* err_base;  // a slot that times out is reported as its offset
+  int64_t err_bias;         // from err_base, plus err_bias
 };
 
-// Input rows of one producer task (tile of S block b, slot q), for the
-// bulk prefetch: q = blockIdx.x + j*gridDim.x is the CTA's j-th slot.
-struct PcTile {
-  const uint8_t* src;  // input row 0 (source PE r)
-  uint32_t rows, len;
+// One task of one S block: the tile of source PE r bound for destination d,
+// expert column h, D block bd.  q = ((d*W + r)*H + h)*nbd + bd.
+struct PcTask {
+  int64_t* slot;       // the signal slot (buffer b % buffer_num) on PE d
+  const uint8_t* src;  // input row d*S + s0 of PE r, at column x0
+  uint8_t* stage;      // staging row 0 of the slot, column r*H + h, x0
+  uint8_t* dst;        // output row s0 of PE d, column r*H + h, x0
+  uint32_t rows;       // rows of the tile (the last S block may be short)
+  uint32_t len;        // bytes per tile row (the last D block may be short)
 };
 
-__device__ __forceinline__ PcTile pc_tile(const PcArgs& a, uint32_t nq, uint64_t t) {
-  const uint32_t b = (uint32_t)(t / nq);
-  size_t q = blockIdx.x + (size_t)(t % nq) * gridDim.x;  // q = ((d*W + r)*H + h)*nbd + bd
+// Task q at S block 0, buffer 0; the other S blocks and buffers are fixed
+// strides from it (PcArgs::tile_src, tile_dst, slot_buf, stage_buf).
+struct PcBase {
+  int64_t* slot;
+  const uint8_t* src;
+  uint8_t* stage;
+  uint8_t* dst;
+  uint32_t len;
+};
+
+__device__ __forceinline__ PcBase pc_base(const PcArgs& a, size_t q) {
   const uint32_t bd = (uint32_t)(q % a.nbd);
   q /= a.nbd;
   const uint32_t h = (uint32_t)(q % a.H);
   q /= a.H;
   const uint32_t r = (uint32_t)(q % a.W);
   const uint32_t d = (uint32_t)(q / a.W);
-  const uint32_t s0 = b * a.tile_s, x0 = bd * a.block_d;
-  PcTile k;
-  k.src = a.in + r * a.slab + (((size_t)(d * a.S + s0) * a.H + h) * a.D + x0) * a.es;
-  k.rows = min(a.tile_s, a.S - s0);
+  const uint32_t x0 = bd * a.block_d;
+  const size_t col = ((size_t)(r * a.H + h) * a.D + x0) * a.es;
+  PcBase k;
+  // slot (0, r, bd, h) of destination d, one 64-byte line each
+  k.slot = reinterpret_cast<int64_t*>(
+      a.signals + d * a.sig_pe + (((size_t)r * a.nbd + bd) * a.H + h) * SYMM_SIGNAL_STRIDE_BYTES);
+  k.src = a.in + r * a.slab + (((size_t)d * a.S * a.H + h) * a.D + x0) * a.es;
+  k.stage = a.staging + d * a.stage_pe + col;
+  k.dst = a.out + d * a.slab + col;
   k.len = min(a.block_d, a.D - x0) * a.es;
   return k;
 }
 
-// Issues the bulk loads of task t's input tile into `tile` (one mbarrier phase).
-__device__ __forceinline__ void pc_prefetch(const PcArgs& a, uint32_t nq, uint64_t t,
-                                            uint8_t* tile, uint64_t* bar) {
-  const PcTile k = pc_tile(a, nq, t);
+__device__ __forceinline__ PcTask pc_task_of(const PcArgs& a, const PcBase& k0, uint32_t b,
+                                             uint32_t buf) {
+  PcTask k;
+  k.slot = reinterpret_cast<int64_t*>(reinterpret_cast<uint8_t*>(k0.slot) + buf * a.slot_buf);
+  k.src = k0.src + b * a.tile_src;
+  k.stage = k0.stage + buf * a.stage_buf;
+  k.dst = k0.dst + b * a.tile_dst;
+  k.rows = min(a.tile_s, a.S - b * a.tile_s);
+  k.len = k0.len;
+  return k;
+}
+
+// CTA c owns the tasks q = c + j*gridDim.x (j < nq) of every S block and
+// walks them S block by S block (the page's fixed core-to-task mapping): its
+// task number t = b*nq + j is task j of S block b, in buffer b % buffer_num.
+__device__ __forceinline__ uint32_t pc_tasks_per_cta(const PcArgs& a) {
+  const size_t per_block = (size_t)a.W * a.W * a.H * a.nbd;
+  return (uint32_t)((per_block - blockIdx.x - 1) / gridDim.x + 1);
+}
+
+// The CTA's tasks decoded once: up to kPcOwned of them in shared memory
+// (the loops then take a task with a few adds and no divisions); more are
+// decoded again at each use.
+constexpr uint32_t kPcOwned = 16;
+struct PcTable {
+  PcBase base[kPcOwned];
+};
+__device__ __forceinline__ void pc_table_fill(const PcArgs& a, uint32_t nq, PcTable& tab) {
+  for (uint32_t j = threadIdx.x; j < nq && j < kPcOwned; j += blockDim.x)
+    tab.base[j] = pc_base(a, blockIdx.x + (size_t)j * gridDim.x);
+}
+__device__ __forceinline__ PcBase pc_table_get(const PcArgs& a, const PcTable& tab, uint32_t j) {
+  return j < kPcOwned ? tab.base[j] : pc_base(a, blockIdx.x + (size_t)j * gridDim.x);
+}
+
+// Position (S block, task, buffer) in a CTA's task sequence, advanced
+// without divisions.
+struct PcCursor {
+  uint32_t b = 0, j = 0, buf = 0;
+  __device__ __forceinline__ void next(uint32_t nq, uint32_t buffer_num) {
+    if (++j == nq) {
+      j = 0;
+      ++b;
+      if (++buf == buffer_num) buf = 0;
+    }
+  }
+};
+__device__ __forceinline__ PcTask pc_task_at(const PcArgs& a, const PcTable& tab,
+                                             const PcCursor& c) {
+  return pc_task_of(a, pc_table_get(a, tab, c.j), c.b, c.buf);
+}
+
+// L2 policies of the producer/consumer copies: SYMM_PC_L2HINT marks the
+// prefetched input reads evict-first and the staging writes evict-last, so
+// streamed input and output lines leave L2 before staged tiles do (measured
+// on GB300, DeepSeek-V3 rows: 5078 against 4986 GB/s, and 476 against 504 MB
+// of DRAM writes at S = 512, fewer staging lines written back).
+#ifndef SYMM_PC_L2HINT
+#define SYMM_PC_L2HINT 1
+#endif
+
+// Issues the bulk loads of a tile's input rows into `tile` (one mbarrier phase).
+__device__ __forceinline__ void pc_prefetch(const PcArgs& a, const PcTask& k, uint8_t* tile,
+                                            uint64_t* bar) {
   const size_t src_row = (size_t)a.H * a.D * a.es;
   symm::mbar_arrive_expect_tx(bar, k.rows * k.len);
-  for (uint32_t i = 0; i < k.rows; ++i)
-    symm::bulk_load(tile + i * k.len, k.src + i * src_row, k.len, bar);
+  if (SYMM_PC_L2HINT) {
+    const uint64_t pol = symm::policy_evict_first();
+    for (uint32_t i = 0; i < k.rows; ++i)
+      symm::bulk_load_hint(tile + i * k.len, k.src + i * src_row, k.len, bar, pol);
+  } else {
+    for (uint32_t i = 0; i < k.rows; ++i)
+      symm::bulk_load(tile + i * k.len, k.src + i * src_row, k.len, bar);
+  }
 }
+
 
 // PREFETCH: the producer group's thread 0 keeps the input tiles of the next
 // kPcPrefetch tasks in flight with bulk (TMA) loads into a shared-memory
@@ -258,69 +360,61 @@ __device__ __forceinline__ void pc_prefetch(const PcArgs& a, uint32_t nq, uint64
 #define SYMM_PC_PREFETCH 2
 #endif
 constexpr int kPcPrefetch = SYMM_PC_PREFETCH;
+
 constexpr uint32_t kPcMaxPrefetchTile = 32 * 1024;
 // Narrowest tile row worth a bulk copy: measured on GB300, rows of 256 B to
 // 1 KB went faster without the prefetch (e.g. 1425 against 936 GB/s on 256 B
 // rows), rows of 2 KB faster with it (4742 against 4302 GB/s).
 constexpr size_t kPcMinPrefetchRow = 2048;
 
-// FLAT: every tile row, base and row stride is 16-byte aligned and a tile
-// spans less than 4 GiB, so whole tiles are copied by symm::group_copy_tile;
-// otherwise row by row with warp_copy (any alignment).
-template <bool PREFETCH, bool FLAT>
+// How a group copies its tile (a tile always spans less than 4 GiB here):
+//   kCopyAligned  every tile row, base and row stride is 16-byte aligned:
+//                 symm::group_copy_tile, the tile flattened to 16-byte vectors;
+//   kCopyAny      the staging and output rows share one 16-byte phase (their
+//                 stride H*W*D*elem_bytes is a multiple of 16), any other
+//                 alignment: symm::group_copy_tile_any, flattened too, with
+//                 funnel-shifted vectors and byte heads and tails;
+//   kCopyRows     anything else: one warp per row with symm::warp_copy.
+enum { kCopyRows = 0, kCopyAligned = 1, kCopyAny = 2 };
+
+template <bool PREFETCH, int MODE>
 __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
     a2a_pc_kernel(const PcArgs a, uint32_t tile_bytes) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int status[2];
+  __shared__ PcTable tab;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int role = warp >> 2;          // 0 = producer group, 1 = consumer group
   const int gwarp = warp & 3;          // warp inside its group
   const int gtid = threadIdx.x & (kPcGroup - 1);
   const int bar_id = 1 + role;         // named barrier of the group
-  const size_t tasks_per_block = (size_t)a.W * a.W * a.H * a.nbd;
   const size_t stage_row = (size_t)a.H * a.W * a.D * a.es;  // one staging row, bytes
-  const uint32_t nq = (uint32_t)((tasks_per_block - blockIdx.x - 1) / gridDim.x + 1);
+  const size_t src_row = (size_t)a.H * a.D * a.es;
+  const uint32_t nq = pc_tasks_per_cta(a);
   const uint64_t ntasks = (uint64_t)a.nbs * nq;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* ring = smem + 128;
+  pc_table_fill(a, nq, tab);
+  __syncthreads();
   uint64_t issued = 0;
+  PcCursor pre;  // the next task whose input the producer prefetches
   if (PREFETCH && role == 0) {
     if (gtid == 0) {
       for (int i = 0; i < kPcPrefetch; ++i) symm::mbar_init(&bars[i], 1);
       symm::fence_mbar_init();
-      for (; issued < ntasks && issued < (uint64_t)kPcPrefetch; ++issued)
-        pc_prefetch(a, nq, issued, ring + issued * tile_bytes, &bars[issued]);
+      for (; issued < ntasks && issued < (uint64_t)kPcPrefetch; ++issued, pre.next(nq, a.buffer_num))
+        pc_prefetch(a, pc_task_at(a, tab, pre), ring + issued * tile_bytes, &bars[issued]);
     }
     symm::group_sync(bar_id, kPcGroup);
   }
 
-  // As on the page, a task (one signal slot) belongs to one CTA for every S
-  // block and the CTA walks the S blocks in order: the producer of S block b
-  // and the consumer of S block b - buffer_num on the same slot are this
-  // CTA's own two groups, so no wait depends on another CTA.
-  uint64_t t = 0;
-  for (uint32_t b = 0; b < a.nbs; ++b)
-  for (size_t q0 = blockIdx.x; q0 < tasks_per_block; q0 += gridDim.x, ++t) {
-    size_t q = q0;  // q = ((d*W + r)*H + h)*nbd + bd
-    const uint32_t bd = (uint32_t)(q % a.nbd);
-    q /= a.nbd;
-    const uint32_t h = (uint32_t)(q % a.H);
-    q /= a.H;
-    const uint32_t r = (uint32_t)(q % a.W);
-    const uint32_t d = (uint32_t)(q / a.W);
-    const uint32_t buf = b % a.buffer_num;
-    // slot (buf, r, bd, h) of destination d, one 64-byte line each
-    int64_t* slot = reinterpret_cast<int64_t*>(
-        a.signals + d * a.slab +
-        ((((size_t)buf * a.W + r) * a.nbd + bd) * a.H + h) * SYMM_SIGNAL_STRIDE_BYTES);
-    const uint32_t s0 = b * a.tile_s;
-    const uint32_t rows = min(a.tile_s, a.S - s0);
-    const uint32_t x0 = bd * a.block_d;
-    const size_t len = (size_t)min(a.block_d, a.D - x0) * a.es;
-    const size_t stage_col = ((size_t)(r * a.H + h) * a.D + x0) * a.es;
-    uint8_t* stage = a.staging + d * a.slab + (size_t)buf * a.tile_s * stage_row + stage_col;
+  // The producer of S block b and the consumer of S block b - buffer_num on
+  // the same slot are this CTA's own two groups, so no wait depends on
+  // another CTA.
+  PcCursor cur;
+  for (uint64_t t = 0; t < ntasks; ++t, cur.next(nq, a.buffer_num)) {
+    const PcTask k = pc_task_at(a, tab, cur);
     const int st = (int)(t % kPcPrefetch);
-
     if (gtid == 0) {
       int rc = symm::kSpinOk;
       if (PREFETCH && role == 0 &&
@@ -329,8 +423,8 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
         rc = symm::kSpinTimeout;
       }
       if (rc == symm::kSpinOk)
-        rc = symm::spin_wait(slot, symm::kCmpEq, role == 0 ? 0 : 1, a.budget_ns, a.ctl,
-                             a.heap_base);
+        rc = symm::spin_wait(k.slot, symm::kCmpEq, role == 0 ? 0 : 1, a.budget_ns, a.ctl,
+                             a.err_base, a.err_bias);
       status[role] = rc;
     }
     symm::group_sync(bar_id, kPcGroup);
@@ -346,45 +440,50 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
       if (PREFETCH) {
         // shared-memory tile -> destination d's slot, 16 bytes per thread-step
         const uint8_t* tile = ring + (size_t)st * tile_bytes;
-        const uint32_t vrow = (uint32_t)(len >> 4), nv = rows * vrow;
+        const uint32_t vrow = k.len >> 4, nv = k.rows * vrow;
+        const uint64_t pol = SYMM_PC_L2HINT ? symm::policy_evict_last() : 0;
         for (uint32_t v = gtid; v < nv; v += kPcGroup) {
           const uint32_t i = v / vrow, c = v - i * vrow;
-          symm::st16(stage + i * stage_row + 16 * c,
-                     *reinterpret_cast<const uint4*>(tile + i * len + 16 * c));
+          const uint4 x = *reinterpret_cast<const uint4*>(tile + i * k.len + 16 * c);
+          if (SYMM_PC_L2HINT)
+            symm::st16_hint(k.stage + i * stage_row + 16 * c, x, pol);
+          else
+            symm::st16(k.stage + i * stage_row + 16 * c, x);
         }
+      } else if (MODE == kCopyAligned) {
+        // input rows d*S + s0 + i of source r -> destination d's slot
+        symm::group_copy_tile<kPcGroup, SYMM_PC_FLAT_UNROLL, symm::kRO, symm::kST>(
+            k.stage, (uint32_t)stage_row, k.src, (uint32_t)src_row, k.rows, k.len >> 4, gtid);
+      } else if (MODE == kCopyAny) {
+        symm::group_copy_tile_any<kPcGroup, SYMM_PC_ANY_UNROLL, symm::kRO, symm::kST>(
+            k.stage, (uint32_t)stage_row, k.src, (uint32_t)src_row, k.rows, k.len, gtid);
       } else {
-        // producer: input rows d*S + s0 + i of source r -> destination d's slot
-        const uint8_t* src =
-            a.in + r * a.slab + (((size_t)(d * a.S + s0) * a.H + h) * a.D + x0) * a.es;
-        const size_t src_row = (size_t)a.H * a.D * a.es;
-        if (FLAT)
-          symm::group_copy_tile<kPcGroup, SYMM_PC_FLAT_UNROLL, symm::kRO, symm::kST>(
-              stage, (uint32_t)stage_row, src, (uint32_t)src_row, rows, (uint32_t)(len >> 4),
-              gtid);
-        else
-          for (uint32_t i = gwarp; i < rows; i += 4)
-            symm::warp_copy<SYMM_PC_UNROLL, symm::kRO, symm::kST>(stage + i * stage_row,
-                                                                   src + i * src_row, len, lane);
+        for (uint32_t i = gwarp; i < k.rows; i += 4)
+          symm::warp_copy<SYMM_PC_UNROLL, symm::kRO, symm::kST>(k.stage + i * stage_row,
+                                                                 k.src + i * src_row, k.len, lane);
       }
     } else {
-      // consumer: staged tile -> output rows s0 + i, column r*H + h
-      uint8_t* dst = a.out + d * a.slab + ((size_t)s0 * a.H * a.W * a.D) * a.es + stage_col;
-      if (FLAT)
+      // staged tile -> output rows s0 + i, column r*H + h
+      if (MODE == kCopyAligned)
         symm::group_copy_tile<kPcGroup, SYMM_PC_FLAT_UNROLL, symm::kCG, symm::kCS>(
-            dst, (uint32_t)stage_row, stage, (uint32_t)stage_row, rows, (uint32_t)(len >> 4),
-            gtid);
+            k.dst, (uint32_t)stage_row, k.stage, (uint32_t)stage_row, k.rows, k.len >> 4, gtid);
+      else if (MODE == kCopyAny)
+        symm::group_copy_tile_any<kPcGroup, SYMM_PC_ANY_UNROLL, symm::kCG, symm::kCS>(
+            k.dst, (uint32_t)stage_row, k.stage, (uint32_t)stage_row, k.rows, k.len, gtid);
       else
-        for (uint32_t i = gwarp; i < rows; i += 4)
-          symm::warp_copy<SYMM_PC_UNROLL, symm::kCG, symm::kCS>(dst + i * stage_row,
-                                                                 stage + i * stage_row, len, lane);
+        for (uint32_t i = gwarp; i < k.rows; i += 4)
+          symm::warp_copy<SYMM_PC_UNROLL, symm::kCG, symm::kCS>(k.dst + i * stage_row,
+                                                                 k.stage + i * stage_row, k.len,
+                                                                 lane);
     }
     symm::group_sync(bar_id, kPcGroup);  // the group's copies precede the release
     if (gtid == 0) {
-      symm::st_release(slot, role == 0 ? 1 : 0);
+      symm::st_release(k.slot, role == 0 ? 1 : 0);
       if (PREFETCH && role == 0 && issued < ntasks) {
         // every producer thread has read this ring slot: refill it
         symm::fence_proxy_async_shared();
-        pc_prefetch(a, nq, issued, ring + (size_t)st * tile_bytes, &bars[st]);
+        pc_prefetch(a, pc_task_at(a, tab, pre), ring + (size_t)st * tile_bytes, &bars[st]);
+        pre.next(nq, a.buffer_num);
         ++issued;
       }
     }
@@ -393,12 +492,13 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
 
 // Zeroes the `slots` signal lines of every PE (the page's host-side reset
 // before each launch, done in-stream).
-__global__ void a2a_signal_reset_kernel(uint8_t* signals, size_t slab, uint32_t W, size_t slots) {
+__global__ void a2a_signal_reset_kernel(uint8_t* signals, size_t sig_pe, uint32_t W,
+                                        size_t slots) {
   const size_t n = (size_t)W * slots;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
     const size_t pe = i / slots, k = i % slots;
-    *reinterpret_cast<int64_t*>(signals + pe * slab + k * SYMM_SIGNAL_STRIDE_BYTES) = 0;
+    *reinterpret_cast<int64_t*>(signals + pe * sig_pe + k * SYMM_SIGNAL_STRIDE_BYTES) = 0;
   }
 }
 
@@ -415,10 +515,21 @@ int resident_ctas(const void* kernel, int threads, size_t smem = 0, size_t smem_
   auto it = cache.find({{dev, kernel}, smem});
   if (it != cache.end()) return it->second;
   if (smem_limit < smem) smem_limit = smem;
-  if (smem_limit > 48 * 1024 &&
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem_limit) != cudaSuccess)
-    return 0;
+  if (smem_limit > 48 * 1024) {
+    // at most what the device lets a CTA opt in to, less the kernel's static part
+    cudaFuncAttributes fa;
+    int optin = 0;
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+      return 0;
+    const size_t most = optin > (int)fa.sharedSizeBytes ? optin - fa.sharedSizeBytes : 0;
+    if (smem > most) return 0;
+    if (smem_limit > most) smem_limit = most;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_limit) != cudaSuccess)
+      return 0;
+  }
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess)
     return 0;
@@ -549,6 +660,91 @@ extern "C" int all2all_pc_workspace(int W, int S, int H, int D, int elem_bytes, 
   return SYMM_OK;
 }
 
+// Zeroes, picks the instance for and launches one producer/consumer combine.
+int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
+  const uint32_t bd = p.block_d ? (uint32_t)p.block_d : (uint32_t)p.D;
+  const uint32_t nbd = (p.D + bd - 1) / bd;
+  if ((uint64_t)std::min(bd, (uint32_t)p.D) * p.es > 0xffffffffull)
+    return fail(SYMM_EINVAL, std::string(what) + ": a tile row (block_d * elem_bytes) exceeds 4 GiB");
+  const size_t slots = (size_t)p.buffer_num * p.W * nbd * p.H;
+  if (p.reset) {
+    const size_t n = slots * p.W;
+    const int grid = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+    a2a_signal_reset_kernel<<<grid, 256, 0, s>>>(p.signals, p.sig_pe, p.W, slots);
+    const int rc = cuda_check(cudaGetLastError(), (std::string(what) + ": signal reset").c_str());
+    if (rc) return rc;
+  }
+  PcArgs a;
+  a.in = p.in;
+  a.out = p.out;
+  a.slab = p.slab;
+  a.staging = p.staging;
+  a.signals = p.signals;
+  a.stage_pe = p.stage_pe;
+  a.sig_pe = p.sig_pe;
+  a.W = p.W;
+  a.H = p.H;
+  a.S = p.S;
+  a.D = p.D;
+  a.es = p.es;
+  a.tile_s = p.tile_s;
+  a.block_d = bd;
+  a.nbd = nbd;
+  a.nbs = (p.S + p.tile_s - 1) / p.tile_s;
+  a.buffer_num = p.buffer_num;
+  a.tile_src = (size_t)p.tile_s * p.H * p.D * p.es;
+  a.tile_dst = (size_t)p.tile_s * p.H * p.W * p.D * p.es;
+  a.stage_buf = a.tile_dst;
+  a.slot_buf = (size_t)p.W * nbd * p.H * SYMM_SIGNAL_STRIDE_BYTES;
+  a.budget_ns = p.budget_ns;
+  a.ctl = static_cast<Control*>(p.ctl);
+  a.err_base = p.err_base;
+  a.err_bias = p.err_bias;
+  // every tile row, base and row stride 16-byte aligned
+  const bool aligned = ((size_t)p.D * p.es) % 16 == 0 && ((size_t)bd * p.es) % 16 == 0 &&
+                       (uintptr_t)p.in % 16 == 0 && (uintptr_t)p.out % 16 == 0 &&
+                       (uintptr_t)p.staging % 16 == 0 && p.slab % 16 == 0 &&
+                       p.stage_pe % 16 == 0;
+  // a tile's offsets fit 32 bits (stage_row = H*W*D*es is its widest row stride)
+  const size_t stage_row = (size_t)p.H * p.W * p.D * p.es;
+  const bool small_tile = (uint64_t)p.tile_s * stage_row < (1ull << 32);
+  // the tile copies a group does (see kCopyAligned, kCopyAny, kCopyRows)
+  const int mode = !small_tile ? kCopyRows
+                   : aligned   ? kCopyAligned
+                   : stage_row % 16 == 0 ? kCopyAny
+                                         : kCopyRows;
+  const size_t tile_bytes = (size_t)p.tile_s * bd * p.es;
+  const size_t tasks = (size_t)p.W * p.W * p.H * nbd;
+  const void* kfn;
+  int threads;
+  size_t smem, smem_limit;
+  {
+    // input prefetch by bulk copies (one per tile row) when every tile row is
+    // 16-byte aligned and at least kPcMinPrefetchRow bytes, and a tile fits
+    // the shared-memory ring; narrower rows are copied faster by the group
+    const bool prefetch = !p.vector_only && mode == kCopyAligned &&
+                          (size_t)bd * p.es >= kPcMinPrefetchRow && tile_bytes <= kPcMaxPrefetchTile;
+    kfn = prefetch                  ? (const void*)a2a_pc_kernel<true, kCopyAligned>
+          : mode == kCopyAligned    ? (const void*)a2a_pc_kernel<false, kCopyAligned>
+          : mode == kCopyAny        ? (const void*)a2a_pc_kernel<false, kCopyAny>
+                                    : (const void*)a2a_pc_kernel<false, kCopyRows>;
+    threads = kPcThreads;
+    smem = prefetch ? 128 + (size_t)kPcPrefetch * tile_bytes : 0;
+    smem_limit = prefetch ? 128 + (size_t)kPcPrefetch * kPcMaxPrefetchTile : 0;
+  }
+  // tasks of one S block, dealt evenly: k per CTA, ceil(tasks / k) CTAs,
+  // never more CTAs than are resident at once (each instance measured on its
+  // own), so every wait is on a CTA that is running
+  const int cap = resident_ctas(kfn, threads, smem, smem_limit);
+  if (cap <= 0) return fail(SYMM_ECUDA, std::string(what) + ": occupancy query failed");
+  const size_t per_cta = (tasks + cap - 1) / cap;
+  const int grid = (int)((tasks + per_cta - 1) / per_cta);
+  uint32_t tb = (uint32_t)tile_bytes;
+  void* args[] = {&a, &tb};
+  return cuda_check(cudaLaunchKernel(kfn, dim3((unsigned)grid), dim3(threads), args, smem, s),
+                    (std::string(what) + ": PC launch").c_str());
+}
+
 static int combine_pc(symm_heap* h, size_t in_off, size_t out_off, size_t nbytes, int W, int S,
                       int H, int D, int es, int flags, int tile_s, int block_d, int buffer_num,
                       void* staging, int64_t* signals, cudaStream_t s) {
@@ -570,65 +766,29 @@ static int combine_pc(symm_heap* h, size_t in_off, size_t out_off, size_t nbytes
   if (nbytes == 0) return SYMM_OK;
   rc = ensure_ctrl(h, s);
   if (rc) return rc;
-
-  const uint32_t bd = block_d ? (uint32_t)block_d : (uint32_t)D;
-  const uint32_t nbd = (D + bd - 1) / bd;
-  const size_t slots = sg_bytes / SYMM_SIGNAL_STRIDE_BYTES;
-  if (!(flags & SYMM_A2A_FLAG_NO_RESET)) {
-    const size_t n = slots * W;
-    const int grid = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
-    a2a_signal_reset_kernel<<<grid, 256, 0, s>>>(h->base + sg_off, h->slab, W, slots);
-    rc = cuda_check(cudaGetLastError(), "all2all_combine: signal reset");
-    if (rc) return rc;
-  }
-  PcArgs a;
-  a.in = h->base + in_off;
-  a.out = h->base + out_off;
-  a.staging = h->base + st_off;
-  a.signals = h->base + sg_off;
-  a.slab = h->slab;
-  a.W = W;
-  a.H = H;
-  a.S = S;
-  a.D = D;
-  a.es = es;
-  a.tile_s = tile_s;
-  a.block_d = bd;
-  a.nbd = nbd;
-  a.nbs = (S + tile_s - 1) / tile_s;
-  a.buffer_num = buffer_num;
-  a.budget_ns = h->spin_budget;
-  a.ctl = reinterpret_cast<Control*>(h->base);
-  a.heap_base = h->base;
-  // stage_row = H*W*D*es is the widest row stride of a tile
-  const bool flat = ((size_t)D * es) % 16 == 0 && ((size_t)bd * es) % 16 == 0 &&
-                    in_off % 16 == 0 && out_off % 16 == 0 && st_off % 16 == 0 &&
-                    (uint64_t)tile_s * H * W * D * es < (1ull << 32);
-  // tasks of one S block, dealt evenly: k per CTA, ceil(tasks / k) CTAs, never
-  // more CTAs than are resident at once
-  const size_t tasks = (size_t)W * W * H * nbd;
-  // input prefetch by bulk copies (one per tile row) when every tile row is
-  // 16-byte aligned and at least kPcMinPrefetchRow bytes, and a tile fits the
-  // shared-memory ring; narrower rows are copied faster by the group itself
-  const size_t tile_bytes = (size_t)tile_s * bd * es;
-  const bool prefetch = !(flags & SYMM_A2A_FLAG_VECTOR) && ((size_t)D * es) % 16 == 0 &&
-                        ((size_t)bd * es) % 16 == 0 && in_off % 16 == 0 &&
-                        (size_t)bd * es >= kPcMinPrefetchRow && tile_bytes <= kPcMaxPrefetchTile;
-  const void* kfn = prefetch ? (flat ? (const void*)a2a_pc_kernel<true, true>
-                                     : (const void*)a2a_pc_kernel<true, false>)
-                            : (flat ? (const void*)a2a_pc_kernel<false, true>
-                                    : (const void*)a2a_pc_kernel<false, false>);
-  const size_t smem = prefetch ? 128 + (size_t)kPcPrefetch * tile_bytes : 0;
-  const int cap = resident_ctas(kfn, kPcThreads, smem,
-                                prefetch ? 128 + (size_t)kPcPrefetch * kPcMaxPrefetchTile : 0);
-  if (cap <= 0) return fail(SYMM_ECUDA, "all2all_combine: occupancy query failed");
-  const size_t per_cta = (tasks + cap - 1) / cap;
-  const int grid = (int)((tasks + per_cta - 1) / per_cta);
-  void* args[] = {&a, nullptr};
-  uint32_t tb = prefetch ? (uint32_t)tile_bytes : 0u;
-  args[1] = &tb;
-  return cuda_check(cudaLaunchKernel(kfn, dim3((unsigned)grid), dim3(kPcThreads), args, smem, s),
-                    "all2all_combine: PC launch");
+  PcPlan p;
+  p.in = h->base + in_off;
+  p.out = h->base + out_off;
+  p.slab = h->slab;
+  p.staging = h->base + st_off;
+  p.stage_pe = h->slab;
+  p.signals = h->base + sg_off;
+  p.sig_pe = h->slab;
+  p.W = W;
+  p.S = S;
+  p.H = H;
+  p.D = D;
+  p.es = es;
+  p.tile_s = tile_s;
+  p.block_d = block_d;
+  p.buffer_num = buffer_num;
+  p.reset = !(flags & SYMM_A2A_FLAG_NO_RESET);
+  p.vector_only = (flags & SYMM_A2A_FLAG_VECTOR) != 0;
+  p.budget_ns = h->spin_budget;
+  p.ctl = h->base;
+  p.err_base = h->base;
+  p.err_bias = 0;
+  return launch_pc(p, s, "all2all_combine");
 }
 
 extern "C" int all2all_combine(symm_heap_t* h, const void* in, void* out, int W, int S, int H,

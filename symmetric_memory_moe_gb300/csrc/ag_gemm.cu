@@ -29,14 +29,8 @@
 //               once and stored to all W PEs' gather_out; the warp that
 //               completes a block (acquire/release count) sets that block's
 //               signal on every PE.
-// When every PE's rows form an even number of 128-row blocks, the CTAs run
-// in two-CTA clusters: the pair computes the tiles of two row blocks that
-// share PE d and columns n0, each CTA loads half of every B slice and the
-// TMA multicast writes it into both CTAs' rings, so B is read from L2 once
-// per pair; a ring stage is refilled once both CTAs' MMAs have released it
-// (their commits arrive on both CTAs' barriers).  The same code runs 2 x 2
-// clusters (A shared by the pairs of column tiles too) when built with
-// SYMM_AG_CLUSTER=4.
+// Every CTA works alone (no thread-block clusters): each loads its own A and
+// B slices into its own shared memory.
 // b is read in place (row-major k x n) as an MN-major operand.  Every wait
 // is bounded; a role that gives up
 // records the error, and the CTA drains its in-flight copies and MMAs before
@@ -75,13 +69,6 @@ constexpr uint32_t kStageBytes = kATile + kBTile;
 #define SYMM_AG_PUSH_WARPS 2
 #endif
 constexpr int kPushWarps = SYMM_AG_PUSH_WARPS;
-// Largest cluster to use: 1 (none), 2 (pairs sharing B) or 4 (2 x 2, pairs
-// sharing A as well).  Pairs measured fastest: on one GB300, RFC example /
-// k = n = 4096, 1193 / 1702 TFLOP/s against 1100 / 1638 for 2 x 2 and
-// 1155 / 1675 for single CTAs.
-#ifndef SYMM_AG_CLUSTER
-#define SYMM_AG_CLUSTER 2
-#endif
 constexpr int kAgThreads = 32 * (6 + kPushWarps);  // TMA, MMA, 4 epilogue, push
 constexpr uint32_t kTmemCols = 2 * kBN;  // two accumulators of kBN fp32 columns
 // epilogue staging: per epilogue warp two 32-row x 64-column output boxes
@@ -131,30 +118,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(symm::smem_addr(bar))
       : "memory");
 }
-// The same box into the same shared-memory offset of every CTA in `mask`
-// (this cluster's CTAs), each completing `bytes` on its own barrier at the
-// offset of `bar`.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int x, int y,
-                                               int z, uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(symm::smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(symm::smem_addr(bar)),
-      "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster; orders what each did before.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
-}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
                                              int z) {
   asm volatile(
@@ -195,14 +158,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    symm::smem_addr(bar))
                : "memory");
-}
-// As tc_commit, arriving on the barrier at `bar`'s offset in every CTA of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(symm::smem_addr(bar)),
-      "h"(mask)
-      : "memory");
 }
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one row per lane).
 // The load and its wait are one asm statement, so no use of the registers
@@ -279,25 +234,17 @@ __device__ __forceinline__ int64_t* ag_counter(const AgArgs& a, uint32_t r, uint
 //                 stays in L2 while the row blocks stream past it (when the
 //                 b matrices do not fit, the first order re-reads them from
 //                 DRAM: 1010 against 1550 TFLOP/s at k = n = 4096).
-// In clusters of CM x CN CTAs, "jb" above stands for a group of CM row blocks
-// and "nt" for a group of CN column tiles; the cluster's member index
-// cm + CM * cn (its rank) is the fastest index.  The CM CTAs with one cn
-// share PE d and columns n0 (one B slice), the CN CTAs with one cm share the
-// rows (one A slice).
 struct AgTile {
   uint32_t d, r, jb, m0, n0;
   bool self;
 };
-template <int CM, int CN>
 __device__ __forceinline__ AgTile ag_tile(const AgArgs& a, uint64_t t) {
   AgTile x;
-  const uint32_t member = (uint32_t)(t % (CM * CN));
-  t /= CM * CN;
-  const uint32_t nb = a.nblk / CM, ntn = a.ntiles_n / CN;
+  const uint32_t nb = a.nblk, ntn = a.ntiles_n;
   const uint64_t n_self = (uint64_t)a.W * nb * ntn;
   const bool self = t < n_self;
   uint64_t v = self ? t : t - n_self;
-  const uint32_t nt = (uint32_t)(v % ntn) * CN + member / CM;
+  const uint32_t nt = (uint32_t)(v % ntn);
   v /= ntn;
   uint32_t jr = 0;
   if (self) {  // (d, jb, nt)
@@ -314,7 +261,6 @@ __device__ __forceinline__ AgTile ag_tile(const AgArgs& a, uint64_t t) {
     x.jb = (uint32_t)(v % nb);
     jr = 1 + (uint32_t)(v / nb);
   }
-  x.jb = x.jb * CM + member % CM;
   x.self = self;
   x.r = (x.d + jr) % a.W;
   x.m0 = x.r * a.m_local + x.jb * kBM;
@@ -333,22 +279,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// The kernel body for clusters of CM x CN CTAs (1 x 1: single CTAs).  The
-// tensor maps are the kernels' __grid_constant__ parameters.
-template <int FMT, int CM, int CN>
-__device__ __forceinline__ void ag_gemm_body(const CUtensorMap& tma_a,
-                                             const CUtensorMap& tma_local,
-                                             const CUtensorMap& tma_b,
-                                             const CUtensorMap& tma_c, const AgArgs& a) {
-  constexpr int MC = CM * CN;
-  if (MC > 1) {  // a launch without this cluster shape gets an error, not multicasts
-    uint32_t n;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-    if (n != (uint32_t)MC || gridDim.x % MC) {
-      if (threadIdx.x == 0) symm::record_error(a.ctl, SYMM_EINVAL, (int64_t)n);
-      return;
-    }
-  }
+// The tensor maps are __grid_constant__ parameters.
+template <int FMT>
+__global__ void __launch_bounds__(kAgThreads, 1)
+    ag_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+                   const __grid_constant__ CUtensorMap tma_local,
+                   const __grid_constant__ CUtensorMap tma_b,
+                   const __grid_constant__ CUtensorMap tma_c, const AgArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (symm::smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -364,7 +301,7 @@ __device__ __forceinline__ void ag_gemm_body(const CUtensorMap& tma_a,
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       symm::mbar_init(&full[s], 1);
-      symm::mbar_init(&empty[s], CM * CN);  // freed by the MMAs of the whole cluster
+      symm::mbar_init(&empty[s], 1);  // freed by this CTA's MMAs
     }
     for (int b = 0; b < 2; ++b) {
       symm::mbar_init(&tfull[b], 1);
@@ -377,19 +314,15 @@ __device__ __forceinline__ void ag_gemm_body(const CUtensorMap& tma_a,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  constexpr uint16_t kAll = (uint16_t)((1u << MC) - 1);
-  const uint32_t rank = MC > 1 ? cluster_rank() : 0;
-  const uint32_t cm = rank % CM, cn = rank / CM;
-  if (MC > 1) cluster_sync();  // the peers' barriers exist before anything lands in them
   const uint32_t tmem = *tmem_slot;
-  const uint32_t G = gridDim.x;  // a multiple of MC: a CTA keeps its member t % MC = rank
+  const uint32_t G = gridDim.x;
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------- TMA producer
       uint64_t it = 0;
       bool ok = true;
       for (uint64_t t = blockIdx.x; ok && t < a.tiles; t += G) {
-        const AgTile x = ag_tile<CM, CN>(a, t);
+        const AgTile x = ag_tile(a, t);
         if (!x.self && symm::spin_wait(ag_signal(a, x.d, x.r, x.jb), symm::kCmpEq, 1, a.budget_ns,
                                        a.ctl, a.heap_base) != symm::kSpinOk) {
           ok = false;
@@ -405,41 +338,19 @@ __device__ __forceinline__ void ag_gemm_body(const CUtensorMap& tma_a,
           }
           uint8_t* st = smem + (size_t)s * kStageBytes;
           symm::mbar_arrive_expect_tx(&full[s], kStageBytes);
-          // A: rows jb*128 .. of a_d itself (own rows) or of the gathered
-          // rows; with CN > 1 this CTA loads 128 / CN of them (the maps' box
-          // height) into every CTA of its row group
+          // A: rows jb*128 .. of a_d itself (own rows) or of the gathered rows
           const CUtensorMap* amap = x.self ? &tma_local : &tma_a;
           const int ay = (int)(x.self ? x.jb * kBM : x.m0);
-          if (CN == 1) {
-            tma_load_3d(st, amap, (int)(kt * kBK), ay, (int)x.d, &full[s]);
-          } else {
-            constexpr uint16_t kRowGroup = (uint16_t)(((1u << (CM * CN)) - 1) / ((1u << CM) - 1));
-            tma_load_3d_mc(st + cn * (kATile / CN), amap, (int)(kt * kBK),
-                           ay + (int)(cn * (kBM / CN)), (int)x.d, &full[s],
-                           (uint16_t)(kRowGroup << cm));
-          }
-          // B: b itself, row-major, in 64 N x kBK K boxes; with CM > 1 this
-          // CTA loads kBN / 64 / CM of them into every CTA of its column group
-          if (CM == 1) {
-            for (int i = 0; i < kBN / 64; ++i)
-              tma_load_3d(st + kATile + i * (kBK * 128), &tma_b, (int)(x.n0 + 64 * i),
-                          (int)(kt * kBK), (int)x.d, &full[s]);
-          } else {
-            constexpr int kShare = kBN / 64 / CM;
-            const uint16_t cols = (uint16_t)(((1u << CM) - 1) << (cn * CM));
-            for (int i = (int)cm * kShare; i < (int)(cm + 1) * kShare; ++i)
-              tma_load_3d_mc(st + kATile + i * (kBK * 128), &tma_b, (int)(x.n0 + 64 * i),
-                             (int)(kt * kBK), (int)x.d, &full[s], cols);
-          }
+          tma_load_3d(st, amap, (int)(kt * kBK), ay, (int)x.d, &full[s]);
+          // B: b itself, row-major, in 64 N x kBK K boxes
+          for (int i = 0; i < kBN / 64; ++i)
+            tma_load_3d(st + kATile + i * (kBK * 128), &tma_b, (int)(x.n0 + 64 * i),
+                        (int)(kt * kBK), (int)x.d, &full[s]);
         }
       }
-      // every load issued lands before the CTA may leave (bounded); in a
-      // cluster, so do the other CTAs' last releases of this CTA's stages
-      for (uint64_t i = it > (uint64_t)kStages ? it - kStages : 0; i < it; ++i) {
+      // every load issued lands before the CTA may leave (bounded)
+      for (uint64_t i = it > (uint64_t)kStages ? it - kStages : 0; i < it; ++i)
         symm::mbar_wait(&full[i % kStages], (uint32_t)((i / kStages) & 1), a.budget_ns);
-        if (MC > 1)
-          symm::mbar_wait(&empty[i % kStages], (uint32_t)((i / kStages) & 1), a.budget_ns);
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {  // -------------------------------------- MMA issuer
@@ -469,10 +380,7 @@ __device__ __forceinline__ void ag_gemm_body(const CUtensorMap& tma_a,
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j)  // K = 16 per instruction (A: +32 bytes)
             tc_mma(acc, ad + 2 * j, bd + kBStep * j, idesc, (kt | j) != 0);
-          if (MC == 1)
-            tc_commit(&empty[s]);
-          else  // the stage is free once both CTAs' MMAs have read it
-            tc_commit_mc(&empty[s], kAll);
+          tc_commit(&empty[s]);
         }
         if (ok) tc_commit(&tfull[buf]);
       }
@@ -490,7 +398,7 @@ __device__ __forceinline__ void ag_gemm_body(const CUtensorMap& tma_a,
     uint8_t* my_stage = out_stage + (size_t)q * 2 * kOutBox;
     uint64_t tc = 0, chunks = 0;
     for (uint64_t t = blockIdx.x; t < a.tiles; t += G, ++tc) {
-      const AgTile x = ag_tile<CM, CN>(a, t);
+      const AgTile x = ag_tile(a, t);
       const uint32_t buf = (uint32_t)(tc & 1);
       if (!mbar_wait_ab(&tfull[buf], (uint32_t)((tc >> 1) & 1), a.budget_ns, a.ctl)) {
         symm::record_error(a.ctl, symm::kErrTimedOut, -6);
@@ -579,28 +487,6 @@ __device__ __forceinline__ void ag_gemm_body(const CUtensorMap& tma_a,
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // No CTA leaves while its peer may still deliver B boxes or MMA arrivals
-  // into its shared memory.
-  if (MC > 1) cluster_sync();
-}
-
-template <int FMT>
-__global__ void __launch_bounds__(kAgThreads, 1)
-    ag_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
-                   const __grid_constant__ CUtensorMap tma_local,
-                   const __grid_constant__ CUtensorMap tma_b,
-                   const __grid_constant__ CUtensorMap tma_c, const AgArgs a) {
-  ag_gemm_body<FMT, 1, 1>(tma_a, tma_local, tma_b, tma_c, a);
-}
-
-// The cluster shape is part of the kernel, so every launch of it has it.
-template <int FMT, int CM, int CN>
-__global__ void __cluster_dims__(CM * CN, 1, 1) __launch_bounds__(kAgThreads, 1)
-    ag_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tma_a,
-                           const __grid_constant__ CUtensorMap tma_local,
-                           const __grid_constant__ CUtensorMap tma_b,
-                           const __grid_constant__ CUtensorMap tma_c, const AgArgs a) {
-  ag_gemm_body<FMT, CM, CN>(tma_a, tma_local, tma_b, tma_c, a);
 }
 
 __global__ void ag_reset_kernel(uint8_t* signals, size_t slab, uint32_t W, uint32_t slots) {
@@ -679,30 +565,20 @@ int ag_shape(int W, int m_local, int k, int n, int block_size, const char* what,
   return SYMM_OK;
 }
 
-// Cluster shapes: mc = 1 (single CTAs), 2 (CM 2 x CN 1: pairs sharing B),
-// 4 (CM 2 x CN 2: pairs sharing B, pairs sharing A).
-const void* ag_kernel(int fmt, int mc) {
-  if (mc == 4)
-    return fmt ? (const void*)ag_gemm_cluster_kernel<1, 2, 2>
-               : (const void*)ag_gemm_cluster_kernel<0, 2, 2>;
-  if (mc == 2)
-    return fmt ? (const void*)ag_gemm_cluster_kernel<1, 2, 1>
-               : (const void*)ag_gemm_cluster_kernel<0, 2, 1>;
+const void* ag_kernel(int fmt) {
   return fmt ? (const void*)ag_gemm_kernel<1> : (const void*)ag_gemm_kernel<0>;
 }
-int ag_cn(int mc) { return mc == 4 ? 2 : 1; }
 
-// CTAs resident at once (one per SM: the kernel takes all of TMEM), in whole
-// clusters of mc CTAs.
-int ag_capacity(int fmt, int mc) {
+// CTAs resident at once (one per SM: the kernel takes all of TMEM).
+int ag_capacity(int fmt) {
   static std::mutex mu;
-  static int cached[2][3][64] = {};
+  static int cached[2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  int& slot = cached[fmt][mc == 4 ? 2 : mc - 1][dev];
+  int& slot = cached[fmt][dev];
   if (slot) return slot;
-  const void* k = ag_kernel(fmt, mc);
+  const void* k = ag_kernel(fmt);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAgSmem) !=
       cudaSuccess)
     return 0;
@@ -710,24 +586,7 @@ int ag_capacity(int fmt, int mc) {
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kAgThreads, kAgSmem) !=
       cudaSuccess)
     return 0;
-  int n = std::min(per_sm, 1) * sm_count();
-  if (mc > 1) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(mc * std::max(n / mc, 1)));
-    cfg.blockDim = dim3(kAgThreads);
-    cfg.dynamicSmemBytes = kAgSmem;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = (unsigned)mc;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess) return 0;
-    n = std::min(n, clusters * mc);
-  }
-  slot = n;
+  slot = std::min(per_sm, 1) * sm_count();
   return slot;
 }
 
@@ -775,23 +634,12 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   rc = ensure_ctrl(h, s);
   if (rc) return rc;
   const int fmt = dtype == SYMM_DTYPE_BF16 ? 1 : 0;
-  // Clusters when the row blocks pair up (an even number per PE), sharing A
-  // as well when the column tiles pair up; single CTAs otherwise.
-  const int ntn = (n + kBN - 1) / kBN;
-  int mc = 1;
-  if (SYMM_AG_CLUSTER >= 2 && sh.nblk % 2 == 0) mc = 2;
-  if (SYMM_AG_CLUSTER >= 4 && mc == 2 && ntn % 2 == 0) mc = 4;
   CUtensorMap map_a, map_local, map_b, map_c;
-  // A boxes are kBM / CN rows high: each CTA of a row group loads its share
-  auto make_a_maps = [&](int cn) {
-    int r = make_map(&map_a, h->base + off[3], fmt, (uint32_t)k, (uint32_t)(W * m_local),
-                     (uint32_t)W, h->slab, kBK, (uint32_t)(kBM / cn));
-    if (!r)
-      r = make_map(&map_local, h->base + off[0], fmt, (uint32_t)k, (uint32_t)m_local, (uint32_t)W,
-                   h->slab, kBK, (uint32_t)(kBM / cn));
-    return r;
-  };
-  rc = make_a_maps(ag_cn(mc));
+  rc = make_map(&map_a, h->base + off[3], fmt, (uint32_t)k, (uint32_t)(W * m_local), (uint32_t)W,
+                h->slab, kBK, kBM);
+  if (rc) return rc;
+  rc = make_map(&map_local, h->base + off[0], fmt, (uint32_t)k, (uint32_t)m_local, (uint32_t)W,
+                h->slab, kBK, kBM);
   if (rc) return rc;
   rc = make_map(&map_b, h->base + off[1], fmt, (uint32_t)n, (uint32_t)k, (uint32_t)W, h->slab, 64,
                 kBK);
@@ -799,8 +647,8 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   rc = make_map(&map_c, h->base + off[2], fmt, (uint32_t)n, (uint32_t)(W * m_local), (uint32_t)W,
                 h->slab, 64, 32);
   if (rc) return rc;
-  const int cap = ag_capacity(fmt, mc);
-  if (cap < mc) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
+  const int cap = ag_capacity(fmt);
+  if (cap < 1) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
 
   ag_reset_kernel<<<(unsigned)std::min<size_t>(((size_t)W * sh.slots * 8 + 255) / 256 + 1, 1024),
                     256, 0, s>>>(h->base + off[4], h->slab, (uint32_t)W, sh.slots);
@@ -830,33 +678,8 @@ extern "C" int shmem_fused_all_gather_matmul(symm_heap_t* h, const void* a, cons
   const int grid = (int)std::min<uint64_t>((uint64_t)cap, std::max<uint64_t>(args.tiles, 1));
   void* kargs[] = {&map_a, &map_local, &map_b, &map_c, &args};
   // cooperative: every CTA resident at once, since tiles wait on blocks that
-  // other CTAs push (the cluster kernels carry their cluster shape)
-  cudaError_t e;
-  if (mc == 1) {
-    e = cudaLaunchCooperativeKernel(ag_kernel(fmt, 1), grid, kAgThreads, kargs, kAgSmem, s);
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(grid / mc * mc));
-    cfg.blockDim = dim3(kAgThreads);
-    cfg.dynamicSmemBytes = kAgSmem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeCooperative;
-    attr.val.cooperative = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelExC(&cfg, ag_kernel(fmt, mc), kargs);
-    if (e != cudaSuccess) {
-      // a configuration the runtime refuses for clusters: single CTAs instead
-      (void)cudaGetLastError();
-      const int cap1 = ag_capacity(fmt, 1);
-      if (cap1 < 1) return fail(SYMM_ECUDA, std::string(what) + ": kernel set-up failed");
-      rc = make_a_maps(1);
-      if (rc) return rc;
-      e = cudaLaunchCooperativeKernel(ag_kernel(fmt, 1),
-                                      (int)std::min<uint64_t>((uint64_t)cap1, args.tiles),
-                                      kAgThreads, kargs, kAgSmem, s);
-    }
-  }
-  return cuda_check(e, "shmem_fused_all_gather_matmul: launch");
+  // other CTAs push
+  return cuda_check(
+      cudaLaunchCooperativeKernel(ag_kernel(fmt), grid, kAgThreads, kargs, kAgSmem, s),
+      "shmem_fused_all_gather_matmul: launch");
 }

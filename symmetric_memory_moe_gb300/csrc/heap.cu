@@ -186,7 +186,12 @@ extern "C" int symm_heap_init(void* base, size_t slab_stride, int npes, symm_hea
   h->next = SYMM_HEAP_HEADER_BYTES;
   h->spin_budget = 2000000000ull;
   h->device = -1;
-  cudaGetDevice(&h->device);
+  if (cudaGetDevice(&h->device) == cudaSuccess) {
+    // set-up of all2all_combine_pc_noalloc on this device: look up its static
+    // array now (this loads the module that holds it), not in its first call
+    uint8_t* scratch = nullptr;
+    (void)symm_host::noalloc_scratch_address(&scratch);
+  }
   cudaGetLastError();  // no device is not an error for host-only use
   h->ctrl_ready = false;
   *heap = h;
@@ -254,9 +259,10 @@ extern "C" int symm_check_error(symm_heap_t* h, void* stream, int64_t* info) {
   const int code = ctl.error ? ctl.error : SYMM_ETIMEDOUT;
   if (code == SYMM_ERANGE)
     return fail(code, "device-side sizes exceed a buffer (nothing was copied)");
-  if (code == SYMM_EINVAL)
-    return fail(code, "a kernel found itself launched without the cluster shape it was built "
-                      "for (clusters of " + std::to_string(ctl.error_info) + " CTAs); it did nothing");
+  if (ctl.error_info >= SYMM_INFO_NOALLOC_SIGNAL)
+    return fail(code, "device wait gave up (signal at byte offset " +
+                          std::to_string(ctl.error_info - SYMM_INFO_NOALLOC_SIGNAL) +
+                          " of the signal area of all2all_combine_pc_noalloc's static array)");
   return fail(code, "device wait gave up (signal at heap byte offset " +
                         std::to_string(ctl.error_info) + ")");
 }

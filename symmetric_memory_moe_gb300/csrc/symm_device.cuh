@@ -87,9 +87,11 @@ __device__ __forceinline__ void record_error(Control* ctl, int code, int64_t inf
   if (atomicCAS(reinterpret_cast<int*>(&ctl->error), 0, code) == 0) ctl->error_info = info;
   st_relaxed_u32(&ctl->abort, 1u);
 }
-__device__ __forceinline__ void record_timeout(Control* ctl, const void* heap_base,
-                                               const int64_t* sig) {
-  record_error(ctl, kErrTimedOut, (int64_t)((const char*)sig - (const char*)heap_base));
+// A wait on `sig` gave up: records its byte offset from `base`, plus `bias`
+// (0 for signals in the heap, whose base is the heap's).
+__device__ __forceinline__ void record_timeout(Control* ctl, const void* base, const int64_t* sig,
+                                               int64_t bias = 0) {
+  record_error(ctl, kErrTimedOut, (int64_t)((const char*)sig - (const char*)base) + bias);
 }
 
 // Longest sleep between two polls of a spin, in ns (0: poll without sleeping).
@@ -100,9 +102,11 @@ __device__ __forceinline__ void record_timeout(Control* ctl, const void* heap_ba
 // Spin (one thread) until `*sig cmp v` holds, with acquire semantics.  Gives
 // up after `budget_ns` of %globaltimer time, or after an iteration cap that
 // bounds the wait even if the timer stood still, or as soon as another waiter
-// has raised the abort flag.  Never traps.
+// has raised the abort flag.  Never traps.  A give-up is recorded as the
+// signal's offset from heap_base plus info_bias.
 __device__ __forceinline__ int spin_wait(const int64_t* sig, int cmp, int64_t v, uint64_t budget_ns,
-                                         Control* ctl, const void* heap_base) {
+                                         Control* ctl, const void* heap_base,
+                                         int64_t info_bias = 0) {
   if (cmp_holds(ld_acquire(sig), cmp, v)) return kSpinOk;
   const uint64_t t0 = globaltimer_ns();
   // a poll takes >= ~16 ns, so this cap is >= ~budget/4 of wall time even if
@@ -113,7 +117,7 @@ __device__ __forceinline__ int spin_wait(const int64_t* sig, int cmp, int64_t v,
     if (cmp_holds(ld_acquire(sig), cmp, v)) return kSpinOk;
     if (ld_relaxed_u32(&ctl->abort)) return kSpinAborted;
     if (globaltimer_ns() - t0 > budget_ns || it > max_iters) {
-      record_timeout(ctl, heap_base, sig);
+      record_timeout(ctl, heap_base, sig, info_bias);
       return kSpinTimeout;
     }
     if (SYMM_SPIN_MAX_SLEEP_NS > 0) {
@@ -164,6 +168,23 @@ __device__ __forceinline__ uint8_t ld1_cg(const uint8_t* p) {
 }
 __device__ __forceinline__ void st1(uint8_t* p, uint8_t v) {
   asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "h"((uint16_t)v) : "memory");
+}
+
+// L2 cache policies (createpolicy) and accesses that carry one.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void st16_hint(void* p, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
 }
 
 // Load policy: kRO for launch-constant inputs, kCG for data written in-launch.
@@ -254,6 +275,71 @@ __device__ __forceinline__ uint4 funnel16(uint4 a, uint4 b, unsigned m) {
     hi = (w1 >> sh) | (w2 << (64 - sh));
   }
   return make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+}
+
+// One tile of rows x len bytes at any alignment, copied by a group of G
+// threads (gtid = 0 .. G-1, whole warps) with the tile flattened to 16-byte
+// output vectors, U in flight per thread.  dst_row must be a multiple of 16,
+// so every row has the same head (bytes before dst's next 16-byte boundary),
+// the same nvec aligned body vectors and the same tail; the source phase may
+// differ from row to row.  A body vector is the funnel shift of the two
+// 16-byte-aligned source blocks under it: the first is loaded, the second
+// comes from the next lane by shuffle when that lane holds the next vector
+// of the same row, and is loaded otherwise (lane 31 and row ends), in the
+// same round as the first.  A block read past a row's last byte stays inside
+// that byte's 16-byte granule.  Head and tail bytes are copied one per
+// thread.  Offsets inside the tile are 32-bit: rows * max(dst_row, src_row)
+// stays below 4 GiB.
+template <int G, int U, int LK, int SK>
+__device__ __forceinline__ void group_copy_tile_any(uint8_t* dst, uint32_t dst_row,
+                                                    const uint8_t* src, uint32_t src_row,
+                                                    uint32_t rows, uint32_t len, int gtid) {
+  uint32_t head = (uint32_t)((16 - ((uintptr_t)dst & 15)) & 15);
+  if (head > len) head = len;
+  const uint32_t nvec = (len - head) >> 4;
+  const uint32_t tail = len - head - (nvec << 4);
+  const uint32_t nv = rows * nvec;
+  const int lane = gtid & 31;
+  for (uint32_t v0 = 0; v0 < nv; v0 += G * U) {  // uniform across the group
+    uint4 a[U], b[U];
+    uint32_t off_d[U], m[U];
+    bool from_next[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t v = v0 + u * G + gtid;
+      const bool valid = v < nv;
+      const uint32_t i = valid ? v / nvec : 0, c = valid ? v - i * nvec : 0;
+      const uint8_t* s = src + (i * src_row + head) + 16 * c;  // first source byte
+      m[u] = (uint32_t)((uintptr_t)s & 15);
+      const uint8_t* blk = s - m[u];
+      off_d[u] = i * dst_row + head + 16 * c;
+      // the next lane holds (i, c + 1) when c + 1 < nvec; lane 31 never does
+      from_next[u] = lane < 31 && c + 1 < nvec;
+      a[u] = valid ? ld16<LK>(blk) : make_uint4(0, 0, 0, 0);
+      b[u] = (valid && m[u] && !from_next[u]) ? ld16<LK>(blk + 16) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t v = v0 + u * G + gtid;
+      uint4 n;
+      n.x = __shfl_down_sync(0xffffffffu, a[u].x, 1);
+      n.y = __shfl_down_sync(0xffffffffu, a[u].y, 1);
+      n.z = __shfl_down_sync(0xffffffffu, a[u].z, 1);
+      n.w = __shfl_down_sync(0xffffffffu, a[u].w, 1);
+      if (from_next[u]) b[u] = n;
+      if (v < nv) st16k<SK>(dst + off_d[u], m[u] ? funnel16(a[u], b[u], m[u]) : a[u]);
+    }
+  }
+  // head and tail bytes (at most 15 + 15): row e >> 5, byte e & 31 of the
+  // row's head | tail
+  const uint32_t edge = head + tail;
+  if (edge)
+    for (uint32_t e = gtid; e < rows * 32; e += G) {
+      const uint32_t i = e >> 5, k = e & 31;
+      if (k >= edge) continue;
+      const uint32_t x = k < head ? k : head + (nvec << 4) + (k - head);
+      st1(dst + i * dst_row + x, ld1<LK>(src + i * src_row + x));
+    }
 }
 
 // ------------------------------------------------------- warp byte copy ---
@@ -367,6 +453,14 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
           "r"(smem_addr(smem_dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load_hint(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                               uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {

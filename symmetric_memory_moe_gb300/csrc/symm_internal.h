@@ -46,4 +46,31 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 int launch_runs_raw(const uint8_t* in, uint8_t* out, size_t in_pe, size_t out_pe, uint32_t W,
                     uint32_t Sb, size_t R, bool inverse, cudaStream_t s, const char* what);
 
+// One producer/consumer combine (all2all_combine's SYMM_A2A_PC and the
+// allocation-free entry point share it): PE k's input and output at
+// in/out + k*slab, its staging ring at staging + k*stage_pe and its signal
+// slots at signals + k*sig_pe.  Shapes as for all2all_combine; the caller
+// has validated them and the ranges.
+struct PcPlan {
+  const uint8_t* in;
+  uint8_t* out;
+  size_t slab;
+  uint8_t* staging;
+  size_t stage_pe;
+  uint8_t* signals;
+  size_t sig_pe;
+  int W, S, H, D, es, tile_s, block_d, buffer_num;
+  bool reset;        // zero the signal slots in-stream before the launch
+  bool vector_only;  // 16-byte vector copies only (SYMM_A2A_FLAG_VECTOR)
+  uint64_t budget_ns;
+  void* ctl;                // the heap header (device) that records errors
+  const uint8_t* err_base;  // a slot that times out is reported as its byte
+  int64_t err_bias;         // offset from err_base plus err_bias
+};
+int launch_pc(const PcPlan& p, cudaStream_t s, const char* what);
+
+// Device address, on the current device, of the static array of
+// all2all_combine_pc_noalloc (looked up once per device and cached).
+int noalloc_scratch_address(uint8_t** out);
+
 }  // namespace symm_host

@@ -42,7 +42,7 @@ def main(argv=None):
     ap.add_argument("--vector", action="store_true",
                     help="pc: 16-byte vector copies only (no bulk prefetch)")
     ap.add_argument("--bulk", action="store_true",
-                    help="direct: bulk (TMA) copies through shared memory")
+                    help="direct and pc: bulk (TMA) copies through shared memory")
     ap.add_argument("--tokens", type=int, default=4096, help="alltoall: tokens per PE")
     ap.add_argument("--experts", type=int, default=256, help="alltoall: routed experts")
     ap.add_argument("--topk", type=int, default=8, help="alltoall: experts per token")
@@ -106,9 +106,22 @@ def main(argv=None):
         raise SystemExit(f"device wait timed out at signal offset {info}")
     ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     moved = 2 * W * bufs.nbytes
+    checked = 0
+    if args.variant in ("direct", "pc", "noalloc"):
+        # sampled runs of the combine: out_d[s, r*H + h] == in_r[d*S + s, h]
+        run = H * D * es
+        outv = heap.views(bufs.out, bufs.nbytes).view(W, S, W, run)
+        inv = heap.views(bufs.inp, bufs.nbytes).view(W, W, S, run)
+        gc = torch.Generator().manual_seed(11)
+        for _ in range(64):
+            d, s, r = (int(torch.randint(0, n, (1,), generator=gc)) for n in (W, S, W))
+            if not torch.equal(outv[d, s, r], inv[r, d, s]):
+                raise SystemExit(f"wrong output run (d={d}, s={s}, r={r})")
+            checked += 1
     print(json.dumps({"variant": args.variant, "W": W, "S": S, "H": H, "D": D, "es": es,
                       "bytes_per_step": moved, "ms": [round(m, 4) for m in ms],
-                      "gbs_median": round(moved / (statistics.median(ms) * 1e-3) / 1e9, 1)}))
+                      "gbs_median": round(moved / (statistics.median(ms) * 1e-3) / 1e9, 1),
+                      "runs_checked": checked}))
     heap.close()
 
 

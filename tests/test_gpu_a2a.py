@@ -193,20 +193,74 @@ def test_unaligned_base_pointers(in_shift, out_shift, variant):
 
 @pytest.mark.parametrize("in_shift,out_shift,tile_s", [
     (0, 0, 8),      # 16-byte-aligned 16 KB tiles: bulk prefetch, whole-tile group copies
-    (0, 8, 8),      # output off 16 bytes: bulk prefetch, row-by-row copies
-    (4, 0, 8),      # input off 16 bytes: no prefetch, row-by-row copies
+    (0, 8, 8),      # output off 16 bytes: group copies with shifted vectors, byte edges
+    (4, 0, 8),      # input off 16 bytes: the same, the source phase off instead
+    (5, 11, 8),     # both off, by different amounts
     (0, 0, 40),     # a tile too big for the prefetch ring: whole-tile group copies
     (16, 48, 40),
+    (3, 0, 40),     # unaligned, tiles taller than the last S block
 ])
 def test_pc_copy_instances(in_shift, out_shift, tile_s):
-    """The producer/consumer kernel's four copy instances, chosen by alignment
-    and tile size, on 2064-byte rows (wide enough for the bulk prefetch) and
-    a ragged last S block (40-row tiles are 81 KB, more than the prefetch
-    ring takes).  Each object leaves 128 bytes of its 256-byte allocation
-    granule free for the shifts."""
+    """The producer/consumer kernel's copy instances, chosen by alignment and
+    tile size, on 2064-byte rows (wide enough for the bulk prefetch) and a
+    ragged last S block (40-row tiles are 81 KB, more than the prefetch ring
+    takes).  Each object leaves 128 bytes of its 256-byte allocation granule
+    free for the shifts."""
     W, S, H, D, es = 4, 45, 2, 1032, 2
     xe = _rand_bytes(W, S * W, H, D, es, seed=tile_s + in_shift).reshape(W, S * W, H, D, es)
     got = _run_es(xe, W, S, H, D, es, "pc", tile_s, 0, 2, in_shift, out_shift)
+    assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
+
+
+@pytest.mark.parametrize("W,S,H,D,es,shift", [
+    (4, 19, 2, 999, 2, 0),    # 1998-byte rows: source phase changes from row to row
+    (4, 19, 2, 999, 2, 6),
+    (8, 9, 1, 15, 2, 0),      # rows shorter than 16 bytes: head and tail bytes only
+    (16, 9, 1, 17, 1, 9),     # 17-byte rows: one vector at most
+    (2, 33, 8, 7, 3, 1),      # 3-byte elements, 21-byte rows
+])
+def test_pc_any_alignment_tiles(W, S, H, D, es, shift):
+    """Tiles whose staging and output rows share one 16-byte phase (H*W*D*es a
+    multiple of 16) but whose rows are not 16-byte aligned: every group
+    copies whole tiles with shifted vectors, on several row lengths and
+    source phases, with tiles of 4 and 32 rows."""
+    xe = _rand_bytes(W, S * W, H, D, es, seed=D * 7 + shift).reshape(W, S * W, H, D, es)
+    for tile_s in (4, 32):
+        got = _run_es(xe, W, S, H, D, es, "pc", tile_s, 0, 2, shift, 0)
+        assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
+
+
+@pytest.mark.parametrize("W,S,H,buf,tile_s", [
+    (2, 24, 1, 1, 4),    # one slot per CTA, one buffer: reused by the very next tile
+    (2, 24, 1, 2, 4),    # two slots in rotation
+    (2, 24, 1, 3, 4),    # three
+    (2, 22, 1, 2, 4),    # ragged last S block
+    (16, 8, 2, 1, 4),    # 512 tasks per S block: CTAs own two or more tasks each
+    (16, 9, 2, 2, 2),
+])
+def test_pc_slot_rotations(W, S, H, buf, tile_s):
+    """2 KB rows (the prefetching instance) with one to three buffers and one
+    or several tasks per CTA: each slot is reused every tasks x buffers tiles
+    of its CTA, from one to several times per S block."""
+    D, es = 1024, 2
+    xe = _rand_bytes(W, S * W, H, D, es, seed=W * 100 + S + buf).reshape(W, S * W, H, D, es)
+    got = _run_es(xe, W, S, H, D, es, "pc", tile_s, 0, buf)
+    assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
+
+
+@pytest.mark.parametrize("D,tile_s,block_d", [
+    (16000, 4, 0),      # 32000-byte rows, 125 KB tiles: no prefetch
+    (7168, 64, 1024),   # tiles of 64 2 KB rows: no prefetch
+    (7168, 2, 0),       # 14 KB rows, 28 KB tiles: prefetched
+    (3000, 8, 1032),    # ragged D blocks (2064 + 2064 + 1872 bytes): prefetched
+])
+def test_pc_wide_rows_and_tall_tiles(D, tile_s, block_d):
+    """Aligned rows of 2 KB to 32 KB: tiles that the input prefetch ring takes
+    (up to 32 KB) and tiles taller than it (copied without the prefetch),
+    with ragged D blocks and S blocks."""
+    W, S, H, es = 4, 37, 1, 2
+    xe = _rand_bytes(W, S * W, H, D, es, seed=D + tile_s).reshape(W, S * W, H, D, es)
+    got = _run_es(xe, W, S, H, D, es, "pc", tile_s, block_d, 2)
     assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
 
 
@@ -225,11 +279,12 @@ def test_empty_extents_are_noops(S, H, D):
     heap.close()
 
 
-def test_repeated_pc_calls_reuse_signals():
+@pytest.mark.parametrize("variant", ["pc", "pc_vec"])
+def test_repeated_pc_calls_reuse_signals(variant):
     """Back-to-back PC launches on one workspace (reset in-stream each time)."""
     W, S, H, D = 4, 24, 2, 40
     x = _rand_bytes(W, S * W, H, D, 2, seed=5).view(torch.int16).reshape(W, S * W, H, D)
-    got = run_combine(x, W, S, H, D, "pc", tile_s=4, block_d=16, repeat=3)
+    got = run_combine(x, W, S, H, D, variant, tile_s=4, block_d=16, repeat=3)
     assert_bits_equal(got, expect_combine(x, W, S, H, D))
 
 

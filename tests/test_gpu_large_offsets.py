@@ -118,4 +118,5 @@ def test_fused_all_gather_matmul(heap):
     gg = heap.download(pg, sizes[3]).view(torch.bfloat16).double().numpy().reshape(gather.shape)
     cc = heap.download(pc, sizes[2]).view(torch.bfloat16).double().numpy().reshape(ref.shape)
     assert np.array_equal(gg, gather)
-    assert (np.abs(cc - ref) <= 2.0 ** -8 * np.abs(ref) + 2.0 ** -12 * mag).all()
+    # bf16 output rounding plus k fp32 additions of at most 2^-23 each
+    assert (np.abs(cc - ref) <= 2.0 ** -8 * np.abs(ref) + (1 + 2.0 ** -8) * k * 2.0 ** -23 * mag).all()
