@@ -67,10 +67,10 @@ namespace {
 #define SYMM_RUNS_GENERAL_MIN_BLOCKS 6
 #endif
 // 16-byte vectors in flight per lane in the row-by-row producer/consumer
-// copies (rows whose staging stride is not a multiple of 16 bytes); 3 is the
-// most that fits the register budget of 3 CTAs per SM without spills
+// copies (rows whose staging stride is not a multiple of 16 bytes); 2 fits
+// the register budget of 3 CTAs per SM without spills
 #ifndef SYMM_PC_UNROLL
-#define SYMM_PC_UNROLL 3
+#define SYMM_PC_UNROLL 2
 #endif
 // 16-byte vectors in flight per thread in the producer/consumer tile copies
 // that spread a whole tile over the group (tiles with 16-byte-aligned rows)
@@ -227,6 +227,7 @@ struct PcArgs {
   size_t tile_dst;   // output bytes from one S block to the next
   size_t stage_buf;  // staging bytes from one buffer to the next
   size_t slot_buf;   // signal bytes from one buffer to the next
+  uint32_t reset;    // zero this launch's signal slots first (each CTA its own)
   uint64_t budget_ns;
   Control* ctl;
   const uint8_t* err_base;  // a slot that times out is reported as its offset
@@ -309,6 +310,20 @@ __device__ __forceinline__ PcBase pc_table_get(const PcArgs& a, const PcTable& t
   return j < kPcOwned ? tab.base[j] : pc_base(a, blockIdx.x + (size_t)j * gridDim.x);
 }
 
+// Zeroes the signal slots of the CTA's tasks, every buffer (the page's reset
+// before each launch, done by each slot's owner: a slot belongs to exactly
+// one task and a task to one CTA, so no other CTA touches it).  gpu-scope
+// stores, then a CTA barrier (the caller's) before any acquire.
+__device__ __forceinline__ void pc_zero_own_slots(const PcArgs& a, uint32_t nq,
+                                                  const PcTable& tab) {
+  for (uint32_t i = threadIdx.x; i < nq * a.buffer_num; i += blockDim.x) {
+    const uint32_t j = i / a.buffer_num, buf = i - j * a.buffer_num;
+    int64_t* slot = reinterpret_cast<int64_t*>(
+        reinterpret_cast<uint8_t*>(pc_table_get(a, tab, j).slot) + buf * a.slot_buf);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(slot), "l"((int64_t)0) : "memory");
+  }
+}
+
 // Position (S block, task, buffer) in a CTA's task sequence, advanced
 // without divisions.
 struct PcCursor {
@@ -360,6 +375,10 @@ __device__ __forceinline__ void pc_prefetch(const PcArgs& a, const PcTask& k, ui
 #define SYMM_PC_PREFETCH 2
 #endif
 constexpr int kPcPrefetch = SYMM_PC_PREFETCH;
+// The prefetching instance with release warps (a2a_pc_rel_kernel, below).
+#ifndef SYMM_PC_RELEASE_WARPS
+#define SYMM_PC_RELEASE_WARPS 1
+#endif
 
 constexpr uint32_t kPcMaxPrefetchTile = 32 * 1024;
 // Narrowest tile row worth a bulk copy: measured on GB300, rows of 256 B to
@@ -396,6 +415,10 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
   uint8_t* ring = smem + 128;
   pc_table_fill(a, nq, tab);
   __syncthreads();
+  if (a.reset) {
+    pc_zero_own_slots(a, nq, tab);
+    __syncthreads();
+  }
   uint64_t issued = 0;
   PcCursor pre;  // the next task whose input the producer prefetches
   if (PREFETCH && role == 0) {
@@ -490,15 +513,209 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
   }
 }
 
-// Zeroes the `slots` signal lines of every PE (the page's host-side reset
-// before each launch, done in-stream).
-__global__ void a2a_signal_reset_kernel(uint8_t* signals, size_t sig_pe, uint32_t W,
-                                        size_t slots) {
-  const size_t n = (size_t)W * slots;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const size_t pe = i / slots, k = i % slots;
-    *reinterpret_cast<int64_t*>(signals + pe * sig_pe + k * SYMM_SIGNAL_STRIDE_BYTES) = 0;
+// ------------------------------- producer / consumer, release warps ---
+// a2a_pc_kernel's prefetching instance with the releases taken off the copy
+// groups.  A gpu-scope release waits for the memory system -- about 2 µs
+// while the GPU streams at HBM rate, measured -- and in a2a_pc_kernel the
+// whole group waits behind it.  Here:
+//   warps 0-3  producer group: thread 0 waits for the tile's input in the
+//              prefetch ring and acquires the slot (== 0); the group copies
+//              the tile into the staging slot and arrives on tile t's done
+//              barrier (one of kPcRelLag that alternate);
+//   warps 4-7  consumer group: thread 0 acquires (== 1), the group copies the
+//              staged tile out and arrives on its done barrier;
+//   warp 8     producer release thread: per tile, waits for done[0], refills
+//              the tile's ring entry with the next input tile, releases the
+//              slot (1) and counts it in released[0];
+//   warp 9     consumer release thread: waits for done[1], releases (0) and
+//              counts it in released[1].
+// A group may acquire tile t only once tile t - min(R, kPcRelLag) is
+// released (R = the CTA's slot rotation, tasks x buffers): the slot of tile
+// t - R then no longer holds the value the group waits for from its last
+// use, and the done barrier of tile t - kPcRelLag (the same one of the
+// kPcRelLag that alternate) has been consumed.  The release is an
+// atomic exchange whose result the count depends on, so the count moves only
+// once the release is performed in L2, where the group's acquire reads.
+// Waits on another role's progress (a release thread on its group, a group on
+// its release thread) have twice the spin budget, so that a stuck slot is
+// what a give-up reports, not a wait that depends on it.
+constexpr int kPcRelThreads = 320;
+#ifndef SYMM_PC_REL_LAG
+#define SYMM_PC_REL_LAG 4
+#endif
+constexpr int kPcRelLag = SYMM_PC_REL_LAG;  // done barriers per group (a power of two)
+static_assert((kPcRelLag & (kPcRelLag - 1)) == 0 && kPcRelLag >= 1, "lag: a power of two");
+
+__device__ __forceinline__ uint64_t atom_exch_release(int64_t* p, int64_t v) {
+  uint64_t old;
+  asm volatile("atom.release.gpu.global.exch.b64 %0, [%1], %2;"
+               : "=l"(old)
+               : "l"(p), "l"(v)
+               : "memory");
+  return old;
+}
+// 0, computed from x so that what uses it waits for x
+__device__ __forceinline__ uint32_t zero_after(uint64_t x) {
+  uint32_t z;
+  asm volatile("{\n\t.reg .b64 t;\n\tand.b64 t, %1, 0;\n\tcvt.u32.u64 %0, t;\n\t}"
+               : "=r"(z)
+               : "l"(x));
+  return z;
+}
+// Bounded wait on an mbarrier phase that also gives up once the heap's abort
+// flag is raised.
+__device__ __forceinline__ bool pc_mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns,
+                                             Control* ctl) {
+  if (symm::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = symm::globaltimer_ns();
+  const uint64_t max_iters = budget_ns / 32 + (1u << 20);
+  for (uint64_t it = 0;; ++it) {
+    if (symm::mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 63 && (symm::ld_relaxed_u32(&ctl->abort) ||
+                            symm::globaltimer_ns() - t0 > budget_ns || it > max_iters))
+      return false;
+  }
+}
+// Bounded wait until a shared-memory count reaches `want`.
+__device__ __forceinline__ bool pc_count_wait(volatile uint32_t* count, uint32_t want,
+                                              uint64_t budget_ns, Control* ctl) {
+  if (*count >= want) return true;
+  const uint64_t t0 = symm::globaltimer_ns();
+  const uint64_t max_iters = budget_ns / 64 + 4096;
+  for (uint64_t it = 0;; ++it) {
+    if (*count >= want) return true;
+    if (symm::ld_relaxed_u32(&ctl->abort)) return false;
+    if (symm::globaltimer_ns() - t0 > budget_ns || it > max_iters) {
+      symm::record_error(ctl, symm::kErrTimedOut, -1);
+      return false;
+    }
+    __nanosleep(32);
+  }
+}
+__device__ __forceinline__ void pc_mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(symm::smem_addr(bar)) : "memory");
+}
+
+// Warps of the producer group (the rest of warps 0-7 form the consumer group).
+#ifndef SYMM_PC_REL_PRODUCER_WARPS
+#define SYMM_PC_REL_PRODUCER_WARPS 4
+#endif
+constexpr int kPcRelPW = SYMM_PC_REL_PRODUCER_WARPS;
+constexpr int kPcRelPG = 32 * kPcRelPW;        // producer group threads
+constexpr int kPcRelCG = 32 * (8 - kPcRelPW);  // consumer group threads
+
+__global__ void __launch_bounds__(kPcRelThreads, kPcMinBlocks)
+    a2a_pc_rel_kernel(const PcArgs a, uint32_t tile_bytes) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int status[2];
+  __shared__ PcTable tab;
+  __shared__ volatile uint32_t released[2];
+  static_assert((kPcPrefetch + 2 * kPcRelLag) * 8 <= 128, "barriers fit the ring's header");
+  uint64_t* in_full = reinterpret_cast<uint64_t*>(smem);  // kPcPrefetch ring barriers
+  uint64_t* done = in_full + kPcPrefetch;                  // [role][t % kPcRelLag]
+  uint8_t* ring = smem + 128;
+  const int warp = threadIdx.x >> 5;
+  // 0 producer group, 1 consumer group, 2 release threads
+  const int role = warp < kPcRelPW ? 0 : (warp < 8 ? 1 : 2);
+  const int gtid = role == 0 ? (int)threadIdx.x : (int)threadIdx.x - kPcRelPG;
+  const int gsize = role == 0 ? kPcRelPG : kPcRelCG;
+  const int bar_id = 1 + role;
+  const size_t stage_row = (size_t)a.H * a.W * a.D * a.es;
+  const uint32_t nq = pc_tasks_per_cta(a);
+  const uint64_t ntasks = (uint64_t)a.nbs * nq;
+  const uint64_t rotation = (uint64_t)nq * a.buffer_num;
+  const uint64_t lag = rotation < (uint64_t)kPcRelLag ? rotation : (uint64_t)kPcRelLag;
+  pc_table_fill(a, nq, tab);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPcPrefetch; ++i) symm::mbar_init(&in_full[i], 1);
+    for (int i = 0; i < kPcRelLag; ++i) {
+      symm::mbar_init(&done[i], kPcRelPG);
+      symm::mbar_init(&done[kPcRelLag + i], kPcRelCG);
+    }
+    released[0] = 0;
+    released[1] = 0;
+    symm::fence_mbar_init();
+  }
+  __syncthreads();
+  if (a.reset) {
+    pc_zero_own_slots(a, nq, tab);
+    __syncthreads();
+  }
+
+  if (role < 2) {  // ------------------------------------ copy groups
+    const uint64_t pol = symm::policy_evict_last();
+    PcCursor cur;
+    for (uint64_t t = 0; t < ntasks; ++t, cur.next(nq, a.buffer_num)) {
+      const PcTask k = pc_task_at(a, tab, cur);
+      const int st = (int)(t % kPcPrefetch);
+      if (gtid == 0) {
+        int rc = symm::kSpinOk;
+        if (t + 1 > lag &&
+            !pc_count_wait(&released[role], (uint32_t)(t + 1 - lag), 2 * a.budget_ns, a.ctl))
+          rc = symm::kSpinTimeout;
+        if (rc == symm::kSpinOk && role == 0 &&
+            !pc_mbar_wait(&in_full[st], (uint32_t)(t / kPcPrefetch) & 1u, a.budget_ns, a.ctl)) {
+          symm::record_error(a.ctl, symm::kErrTimedOut, -1);
+          rc = symm::kSpinTimeout;
+        }
+        if (rc == symm::kSpinOk)
+          rc = symm::spin_wait(k.slot, symm::kCmpEq, role == 0 ? 0 : 1, a.budget_ns, a.ctl,
+                               a.err_base, a.err_bias);
+        status[role] = rc;
+      }
+      symm::group_sync(bar_id, gsize);
+      if (status[role] != symm::kSpinOk) return;  // uniform across the group
+      if (role == 0) {
+        const uint8_t* tile = ring + (size_t)st * tile_bytes;
+        const uint32_t vrow = k.len >> 4, nv = k.rows * vrow;
+        for (uint32_t v = gtid; v < nv; v += kPcRelPG) {
+          const uint32_t i = v / vrow, c = v - i * vrow;
+          symm::st16_hint(k.stage + i * stage_row + 16 * c,
+                          *reinterpret_cast<const uint4*>(tile + i * k.len + 16 * c), pol);
+        }
+      } else {
+        symm::group_copy_tile<kPcRelCG, SYMM_PC_FLAT_UNROLL, symm::kCG, symm::kCS>(
+            k.dst, (uint32_t)stage_row, k.stage, (uint32_t)stage_row, k.rows, k.len >> 4, gtid);
+      }
+      pc_mbar_arrive(&done[role * kPcRelLag + (t % kPcRelLag)]);  // this thread's copies precede it
+    }
+  } else if (threadIdx.x == 256) {  // ---------------- producer release thread
+    uint64_t issued = 0;
+    PcCursor pre;
+    for (; issued < ntasks && issued < (uint64_t)kPcPrefetch; ++issued, pre.next(nq, a.buffer_num))
+      pc_prefetch(a, pc_task_at(a, tab, pre), ring + issued * tile_bytes, &in_full[issued]);
+    PcCursor cur;
+    uint64_t t = 0;
+    for (; t < ntasks; ++t, cur.next(nq, a.buffer_num)) {
+      if (!pc_mbar_wait(&done[t % kPcRelLag], (uint32_t)(t / kPcRelLag) & 1u, 2 * a.budget_ns,
+                        a.ctl)) {
+        symm::record_error(a.ctl, symm::kErrTimedOut, -1);
+        break;
+      }
+      if (issued < ntasks) {  // the group has read tile t's ring entry: refill it
+        symm::fence_proxy_async_shared();
+        pc_prefetch(a, pc_task_at(a, tab, pre), ring + (size_t)(t % kPcPrefetch) * tile_bytes,
+                    &in_full[t % kPcPrefetch]);
+        pre.next(nq, a.buffer_num);
+        ++issued;
+      }
+      const uint64_t old = atom_exch_release(pc_task_at(a, tab, cur).slot, 1);
+      released[0] = (uint32_t)(t + 1) + zero_after(old);
+    }
+    // let the loads still in flight land before the CTA may leave (bounded)
+    for (uint64_t i = t; i < issued; ++i)
+      symm::mbar_wait(&in_full[i % kPcPrefetch], (uint32_t)(i / kPcPrefetch) & 1u, a.budget_ns);
+  } else if (threadIdx.x == 288) {  // ---------------- consumer release thread
+    PcCursor cur;
+    for (uint64_t t = 0; t < ntasks; ++t, cur.next(nq, a.buffer_num)) {
+      if (!pc_mbar_wait(&done[kPcRelLag + (t % kPcRelLag)], (uint32_t)(t / kPcRelLag) & 1u,
+                        2 * a.budget_ns, a.ctl)) {
+        symm::record_error(a.ctl, symm::kErrTimedOut, -1);
+        break;
+      }
+      const uint64_t old = atom_exch_release(pc_task_at(a, tab, cur).slot, 0);
+      released[1] = (uint32_t)(t + 1) + zero_after(old);
+    }
   }
 }
 
@@ -666,14 +883,6 @@ int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
   const uint32_t nbd = (p.D + bd - 1) / bd;
   if ((uint64_t)std::min(bd, (uint32_t)p.D) * p.es > 0xffffffffull)
     return fail(SYMM_EINVAL, std::string(what) + ": a tile row (block_d * elem_bytes) exceeds 4 GiB");
-  const size_t slots = (size_t)p.buffer_num * p.W * nbd * p.H;
-  if (p.reset) {
-    const size_t n = slots * p.W;
-    const int grid = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
-    a2a_signal_reset_kernel<<<grid, 256, 0, s>>>(p.signals, p.sig_pe, p.W, slots);
-    const int rc = cuda_check(cudaGetLastError(), (std::string(what) + ": signal reset").c_str());
-    if (rc) return rc;
-  }
   PcArgs a;
   a.in = p.in;
   a.out = p.out;
@@ -692,6 +901,7 @@ int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
   a.nbd = nbd;
   a.nbs = (p.S + p.tile_s - 1) / p.tile_s;
   a.buffer_num = p.buffer_num;
+  a.reset = p.reset ? 1u : 0u;
   a.tile_src = (size_t)p.tile_s * p.H * p.D * p.es;
   a.tile_dst = (size_t)p.tile_s * p.H * p.W * p.D * p.es;
   a.stage_buf = a.tile_dst;
@@ -731,6 +941,10 @@ int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
     threads = kPcThreads;
     smem = prefetch ? 128 + (size_t)kPcPrefetch * tile_bytes : 0;
     smem_limit = prefetch ? 128 + (size_t)kPcPrefetch * kPcMaxPrefetchTile : 0;
+    if (prefetch && SYMM_PC_RELEASE_WARPS) {
+      kfn = (const void*)a2a_pc_rel_kernel;
+      threads = kPcRelThreads;
+    }
   }
   // tasks of one S block, dealt evenly: k per CTA, ceil(tasks / k) CTAs,
   // never more CTAs than are resident at once (each instance measured on its

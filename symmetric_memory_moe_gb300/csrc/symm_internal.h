@@ -60,7 +60,7 @@ struct PcPlan {
   uint8_t* signals;
   size_t sig_pe;
   int W, S, H, D, es, tile_s, block_d, buffer_num;
-  bool reset;        // zero the signal slots in-stream before the launch
+  bool reset;        // zero the signal slots first (inside the launch, each CTA its own)
   bool vector_only;  // 16-byte vector copies only (SYMM_A2A_FLAG_VECTOR)
   uint64_t budget_ns;
   void* ctl;                // the heap header (device) that records errors

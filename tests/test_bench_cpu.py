@@ -16,7 +16,7 @@ def _entry(kernel):
 
 
 def test_committed_traffic_matches_the_current_sources():
-    for kernel in ("a2a_runs_kernel", "a2a_pc_kernel"):
+    for kernel in ("a2a_runs_kernel", "a2a_pc_rel_kernel"):
         e = _entry(kernel)
         assert e["sources_hash"] == bench._kernel_sources_hash(e["sources"]), kernel
         (a0, d0), (a1, d1) = [(c["algorithmic_bytes"], c["dram_bytes"]) for c in e["captures"]]

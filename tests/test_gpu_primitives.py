@@ -119,12 +119,17 @@ def test_wait_on_unset_signal_times_out(heap, cmp, value):
     assert abi.symm_check_error(heap.handle) == (abi.SYMM_OK, 0)
 
 
-def test_pc_stale_signal_times_out_then_recovers():
+@pytest.mark.parametrize("H,D", [
+    (2, 64),      # 128-byte rows: whole-tile group copies, no prefetch
+    (1, 1024),    # 2 KB rows: the prefetching kernel with release threads
+    (2, 999),     # 1998-byte rows: shift-merged group copies
+])
+def test_pc_stale_signal_times_out_then_recovers(H, D):
     """A producer/consumer slot left at a value nobody expects (2): with the
-    in-stream reset skipped, its producer (waits for 0) and consumer (waits
-    for 1) give up after the budget and every other group aborts; the next
-    call with the reset runs clean and bit-exact."""
-    Wp, S, H, D = 4, 32, 2, 64
+    launch's slot reset skipped, its producer (waits for 0) and consumer
+    (waits for 1) give up after the budget and every other group and release
+    thread aborts; the next call with the reset runs clean and bit-exact."""
+    Wp, S = 4, 32
     bufs = CombineBuffers(Wp, S * Wp, H, D, 2, pc=True, S=S, tile_s=8)
     heap = bufs.heap
     g = torch.Generator().manual_seed(3)
@@ -132,7 +137,7 @@ def test_pc_stale_signal_times_out_then_recovers():
     heap.upload(bufs.inp, x.reshape(Wp, -1))
     heap.views(bufs.signals, bufs.signal_bytes).zero_()
     abi.symm_set_spin_budget(heap.handle, 50_000_000)
-    slot = 5  # ((buf*W + r)*nbd + bd)*H + h with buf 0, source r 2, block 0, h 1; on PE 2
+    slot = 2 * H + H - 1  # ((buf*W + r)*nbd + bd)*H + h with buf 0, source r 2, block 0, h H-1; on PE 2
     abi.shmem_signal_op(heap.handle, bufs.signals, slot * 8, 2, abi.SYMM_SIGNAL_SET, 2)
     abi.all2all_combine(heap.handle, bufs.inp, bufs.out, Wp, S, H, D, 2,
                         abi.SYMM_A2A_PC | abi.SYMM_A2A_FLAG_NO_RESET, 8, 0, 2, bufs.staging,
