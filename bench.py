@@ -315,9 +315,11 @@ def cpu_baseline(wl, min_s: float = 8.0) -> dict:
         line["parallel_unavailable"] = str(e)[:200]
         return line
     line.update({"value": round(many, 4), "cores": threads,
-                 "sample": line["sample"].replace("one thread", "") +
-                 f"; OpenMP build over the {wl.W} destinations on {threads} threads: "
-                 f"median of {runsn} runs ({secn:.2f} s each)",
+                 "sample": f"oracle combine on W={wl.W} S={rows} H={wl.H} D={wl.D} bf16 ({rows}/"
+                           f"{wl.S} of the tokens, {moved / 1e9:.3f} GB moved): its OpenMP build "
+                           f"over the {wl.W} destinations on {threads} threads, median of {runsn} "
+                           f"runs ({secn:.2f} s each); the plain build on one thread, median of "
+                           f"{runs1} runs ({sec1:.2f} s each)",
                  "single_thread": {"value": round(one, 4), "unit": UNIT, "cores": 1}})
     return line
 
