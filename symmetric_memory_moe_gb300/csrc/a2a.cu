@@ -465,8 +465,9 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
         const uint8_t* tile = ring + (size_t)st * tile_bytes;
         const uint32_t vrow = k.len >> 4, nv = k.rows * vrow;
         const uint64_t pol = SYMM_PC_L2HINT ? symm::policy_evict_last() : 0;
-        for (uint32_t v = gtid; v < nv; v += kPcGroup) {
-          const uint32_t i = v / vrow, c = v - i * vrow;
+        const symm::TileStep step = symm::tile_step(kPcGroup, vrow);
+        uint32_t i = (uint32_t)gtid / vrow, c = (uint32_t)gtid - i * vrow;
+        for (uint32_t v = gtid; v < nv; v += kPcGroup, step.advance(i, c, vrow)) {
           const uint4 x = *reinterpret_cast<const uint4*>(tile + i * k.len + 16 * c);
           if (SYMM_PC_L2HINT)
             symm::st16_hint(k.stage + i * stage_row + 16 * c, x, pol);
@@ -668,8 +669,9 @@ __global__ void __launch_bounds__(kPcRelThreads, kPcMinBlocks)
       if (role == 0) {
         const uint8_t* tile = ring + (size_t)st * tile_bytes;
         const uint32_t vrow = k.len >> 4, nv = k.rows * vrow;
-        for (uint32_t v = gtid; v < nv; v += kPcRelPG) {
-          const uint32_t i = v / vrow, c = v - i * vrow;
+        const symm::TileStep step = symm::tile_step(kPcRelPG, vrow);
+        uint32_t i = (uint32_t)gtid / vrow, c = (uint32_t)gtid - i * vrow;
+        for (uint32_t v = gtid; v < nv; v += kPcRelPG, step.advance(i, c, vrow)) {
           symm::st16_hint(k.stage + i * stage_row + 16 * c,
                           *reinterpret_cast<const uint4*>(tile + i * k.len + 16 * c), pol);
         }

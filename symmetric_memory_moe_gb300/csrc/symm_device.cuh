@@ -231,6 +231,27 @@ __device__ __forceinline__ void warp_copy_aligned(uint8_t* dst, const uint8_t* s
     if (j + 32 * u < nvec) st16k<SK>(dst + 16 * (j + 32 * u), v[u]);
 }
 
+// A step of `g` vectors through a tile of rows of `vrow` vectors, as whole
+// rows plus vectors (vrow > 0): advance() moves a (row, vector) position by
+// it with two adds and a compare.
+struct TileStep {
+  uint32_t rows, vecs;  // g = rows * vrow + vecs, vecs < vrow
+  __device__ __forceinline__ void advance(uint32_t& i, uint32_t& c, uint32_t vrow) const {
+    i += rows;
+    c += vecs;
+    if (c >= vrow) {
+      c -= vrow;
+      ++i;
+    }
+  }
+};
+__device__ __forceinline__ TileStep tile_step(uint32_t g, uint32_t vrow) {
+  TileStep t;
+  t.rows = g / vrow;
+  t.vecs = g - t.rows * vrow;
+  return t;
+}
+
 // One tile (rows x vrow 16-byte vectors, rows dst_row / src_row bytes apart)
 // copied by a group of G threads (gtid = 0 .. G-1) with the tile flattened
 // to vectors, so narrow rows still keep every thread busy; U vectors in
@@ -241,15 +262,20 @@ __device__ __forceinline__ void group_copy_tile(uint8_t* dst, uint32_t dst_row,
                                                 const uint8_t* src, uint32_t src_row,
                                                 uint32_t rows, uint32_t vrow, int gtid) {
   const uint32_t nv = rows * vrow;
+  if (nv == 0) return;
+  // (row, vector) of this thread's next vector, and the step of G vectors,
+  // kept by adds: two divisions per call instead of one per vector, so the
+  // loads of a round do not wait on a division chain
+  const TileStep step = tile_step(G, vrow);
+  uint32_t i = (uint32_t)gtid / vrow, c = (uint32_t)gtid - i * vrow;
   for (uint32_t v0 = gtid; v0 < nv; v0 += G * U) {
     uint4 x[U];
     uint32_t off_d[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint32_t v = v0 + u * G;
-      const uint32_t i = v / vrow, c = v - i * vrow;
       off_d[u] = i * dst_row + 16 * c;
-      if (v < nv) x[u] = ld16<LK>(src + (i * src_row + 16 * c));
+      if (v0 + u * G < nv) x[u] = ld16<LK>(src + (i * src_row + 16 * c));
+      step.advance(i, c, vrow);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -300,6 +326,9 @@ __device__ __forceinline__ void group_copy_tile_any(uint8_t* dst, uint32_t dst_r
   const uint32_t tail = len - head - (nvec << 4);
   const uint32_t nv = rows * nvec;
   const int lane = gtid & 31;
+  // (row, vector) of this thread's next vector, advanced by adds (see group_copy_tile)
+  const TileStep step = nvec ? tile_step(G, nvec) : TileStep{0, 0};
+  uint32_t i = nvec ? (uint32_t)gtid / nvec : 0, c = nvec ? (uint32_t)gtid - i * nvec : 0;
   for (uint32_t v0 = 0; v0 < nv; v0 += G * U) {  // uniform across the group
     uint4 a[U], b[U];
     uint32_t off_d[U], m[U];
@@ -308,8 +337,7 @@ __device__ __forceinline__ void group_copy_tile_any(uint8_t* dst, uint32_t dst_r
     for (int u = 0; u < U; ++u) {
       const uint32_t v = v0 + u * G + gtid;
       const bool valid = v < nv;
-      const uint32_t i = valid ? v / nvec : 0, c = valid ? v - i * nvec : 0;
-      const uint8_t* s = src + (i * src_row + head) + 16 * c;  // first source byte
+      const uint8_t* s = src + (i * src_row + head) + 16 * c;  // first source byte (if valid)
       m[u] = (uint32_t)((uintptr_t)s & 15);
       const uint8_t* blk = s - m[u];
       off_d[u] = i * dst_row + head + 16 * c;
@@ -317,6 +345,7 @@ __device__ __forceinline__ void group_copy_tile_any(uint8_t* dst, uint32_t dst_r
       from_next[u] = lane < 31 && c + 1 < nvec;
       a[u] = valid ? ld16<LK>(blk) : make_uint4(0, 0, 0, 0);
       b[u] = (valid && m[u] && !from_next[u]) ? ld16<LK>(blk + 16) : make_uint4(0, 0, 0, 0);
+      step.advance(i, c, nvec);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
