@@ -228,6 +228,7 @@ struct PcArgs {
   size_t stage_buf;  // staging bytes from one buffer to the next
   size_t slot_buf;   // signal bytes from one buffer to the next
   uint32_t reset;    // zero this launch's signal slots first (each CTA its own)
+  uint32_t discard;  // drop a slot's staging lines from L2 after its last use
   uint64_t budget_ns;
   Control* ctl;
   const uint8_t* err_base;  // a slot that times out is reported as its offset
@@ -287,9 +288,18 @@ __device__ __forceinline__ PcTask pc_task_of(const PcArgs& a, const PcBase& k0, 
   return k;
 }
 
-// CTA c owns the tasks q = c + j*gridDim.x (j < nq) of every S block and
-// walks them S block by S block (the page's fixed core-to-task mapping): its
-// task number t = b*nq + j is task j of S block b, in buffer b % buffer_num.
+// CTA c owns the tasks q = c + j*gridDim.x (j < nq) of every S block (the
+// page's fixed core-to-task mapping), and walks them task by task: its tile
+// number t = j*nbs + b is S block b of task j, in buffer b % buffer_num.  A
+// slot's successive producers are then one CTA, in S-block order, as on the
+// page, whose cores walk S block by S block instead; with several tasks per
+// CTA that order keeps every task's slots in use at once (the whole staging
+// ring), this one only each CTA's current task's buffer_num slots, which
+// L2 can hold.  SYMM_PC_TASK_MAJOR = 0 selects the page's order
+// (t = b*nq + j).
+#ifndef SYMM_PC_TASK_MAJOR
+#define SYMM_PC_TASK_MAJOR 1
+#endif
 __device__ __forceinline__ uint32_t pc_tasks_per_cta(const PcArgs& a) {
   const size_t per_block = (size_t)a.W * a.W * a.H * a.nbd;
   return (uint32_t)((per_block - blockIdx.x - 1) / gridDim.x + 1);
@@ -328,14 +338,26 @@ __device__ __forceinline__ void pc_zero_own_slots(const PcArgs& a, uint32_t nq,
 // without divisions.
 struct PcCursor {
   uint32_t b = 0, j = 0, buf = 0;
-  __device__ __forceinline__ void next(uint32_t nq, uint32_t buffer_num) {
-    if (++j == nq) {
+  __device__ __forceinline__ void next(uint32_t nq, uint32_t nbs, uint32_t buffer_num) {
+    if (SYMM_PC_TASK_MAJOR) {
+      if (++b == nbs) {
+        b = 0;
+        buf = 0;
+        ++j;
+      } else if (++buf == buffer_num) {
+        buf = 0;
+      }
+    } else if (++j == nq) {
       j = 0;
       ++b;
       if (++buf == buffer_num) buf = 0;
     }
   }
 };
+// Fewest tiles between two uses of one slot in a CTA's sequence.
+__device__ __forceinline__ uint64_t pc_slot_reuse(uint32_t nq, uint32_t buffer_num) {
+  return SYMM_PC_TASK_MAJOR ? (uint64_t)buffer_num : (uint64_t)nq * buffer_num;
+}
 __device__ __forceinline__ PcTask pc_task_at(const PcArgs& a, const PcTable& tab,
                                              const PcCursor& c) {
   return pc_task_of(a, pc_table_get(a, tab, c.j), c.b, c.buf);
@@ -385,6 +407,12 @@ constexpr uint32_t kPcMaxPrefetchTile = 32 * 1024;
 // 1 KB went faster without the prefetch (e.g. 1425 against 936 GB/s on 256 B
 // rows), rows of 2 KB faster with it (4742 against 4302 GB/s).
 constexpr size_t kPcMinPrefetchRow = 2048;
+// The same for rows of any alignment, whose copies without the prefetch
+// shift-merge two loaded blocks per vector (a2a_pc_rel_kernel<true>).
+#ifndef SYMM_PC_ANY_PREFETCH
+#define SYMM_PC_ANY_PREFETCH 1
+#endif
+constexpr size_t kPcMinPrefetchRowAny = 1024;
 
 // How a group copies its tile (a tile always spans less than 4 GiB here):
 //   kCopyAligned  every tile row, base and row stride is 16-byte aligned:
@@ -425,7 +453,7 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
     if (gtid == 0) {
       for (int i = 0; i < kPcPrefetch; ++i) symm::mbar_init(&bars[i], 1);
       symm::fence_mbar_init();
-      for (; issued < ntasks && issued < (uint64_t)kPcPrefetch; ++issued, pre.next(nq, a.buffer_num))
+      for (; issued < ntasks && issued < (uint64_t)kPcPrefetch; ++issued, pre.next(nq, a.nbs, a.buffer_num))
         pc_prefetch(a, pc_task_at(a, tab, pre), ring + issued * tile_bytes, &bars[issued]);
     }
     symm::group_sync(bar_id, kPcGroup);
@@ -435,7 +463,7 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
   // the same slot are this CTA's own two groups, so no wait depends on
   // another CTA.
   PcCursor cur;
-  for (uint64_t t = 0; t < ntasks; ++t, cur.next(nq, a.buffer_num)) {
+  for (uint64_t t = 0; t < ntasks; ++t, cur.next(nq, a.nbs, a.buffer_num)) {
     const PcTask k = pc_task_at(a, tab, cur);
     const int st = (int)(t % kPcPrefetch);
     if (gtid == 0) {
@@ -507,7 +535,7 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
         // every producer thread has read this ring slot: refill it
         symm::fence_proxy_async_shared();
         pc_prefetch(a, pc_task_at(a, tab, pre), ring + (size_t)st * tile_bytes, &bars[st]);
-        pre.next(nq, a.buffer_num);
+        pre.next(nq, a.nbs, a.buffer_num);
         ++issued;
       }
     }
@@ -519,33 +547,150 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
 // groups.  A gpu-scope release waits for the memory system -- about 2 µs
 // while the GPU streams at HBM rate, measured -- and in a2a_pc_kernel the
 // whole group waits behind it.  Here:
-//   warps 0-3  producer group: thread 0 waits for the tile's input in the
-//              prefetch ring and acquires the slot (== 0); the group copies
-//              the tile into the staging slot and arrives on tile t's done
-//              barrier (one of kPcRelLag that alternate);
+//   warps 0-3  producer group: thread 0 acquires the slot (== 0); for each
+//              input chunk of the tile (below) thread 0 waits for the chunk
+//              in the prefetch ring, the group copies it into the staging
+//              slot and arrives on the chunk's done barrier (one of
+//              kPcRelLag that alternate);
 //   warps 4-7  consumer group: thread 0 acquires (== 1), the group copies the
-//              staged tile out and arrives on its done barrier;
-//   warp 8     producer release thread: per tile, waits for done[0], refills
-//              the tile's ring entry with the next input tile, releases the
-//              slot (1) and counts it in released[0];
-//   warp 9     consumer release thread: waits for done[1], releases (0) and
-//              counts it in released[1].
+//              staged tile out and arrives on the tile's done barrier;
+//   warp 8     producer release thread: per chunk, waits for its done
+//              barrier and refills its ring entry with the next input chunk;
+//              after a tile's last chunk, releases the slot (1) and counts it
+//              in released[0];
+//   warp 9     consumer release warp: per tile, waits for done[1], drops the
+//              staging lines of a slot's last use from L2 when
+//              PcArgs::discard is set (below), releases (0) and counts it
+//              in released[1].
 // A group may acquire tile t only once tile t - min(R, kPcRelLag) is
-// released (R = the CTA's slot rotation, tasks x buffers): the slot of tile
-// t - R then no longer holds the value the group waits for from its last
-// use, and the done barrier of tile t - kPcRelLag (the same one of the
-// kPcRelLag that alternate) has been consumed.  The release is an
-// atomic exchange whose result the count depends on, so the count moves only
-// once the release is performed in L2, where the group's acquire reads.
-// Waits on another role's progress (a release thread on its group, a group on
-// its release thread) have twice the spin budget, so that a stuck slot is
-// what a give-up reports, not a wait that depends on it.
+// released (R = the fewest tiles between two uses of a slot in the CTA's
+// sequence: buffer_num when it walks task by task, tasks x buffers when S
+// block by S block): the slot of tile t - R then no longer holds the value
+// the group waits for from its last use, and the done barrier of tile
+// t - kPcRelLag (the same one of the kPcRelLag that alternate) has been
+// consumed.  The producer group reuses a
+// done barrier per chunk; it is never more than kPcRelPrefetch chunks ahead
+// of its release thread (a chunk's ring entry is refilled only after the
+// chunk kPcRelPrefetch earlier is done), so kPcRelLag >= kPcRelPrefetch
+// keeps those phases apart too.  The release is an atomic exchange whose
+// result the count depends on, so the count moves only once the release is
+// performed in L2, where the group's acquire reads.  Waits on another role's
+// progress (a release thread on its group, a group on its release thread)
+// have twice the spin budget, so that a stuck slot is what a give-up
+// reports, not a wait that depends on it.
+//
+// Input chunks: a tile's input rows arrive in chunks of up to
+// PcRing::chunk_rows rows, one ring entry each, so a tile taller than a ring
+// entry still streams through the ring.
+//   ANY = false  16-byte-aligned rows, loaded as they are and packed in the
+//                entry (row pitch = the row's bytes); both groups copy
+//                aligned 16-byte vectors.
+//   ANY = true   rows of any alignment whose staging and output rows share
+//                one 16-byte phase.  Bulk copies need 16-byte-aligned
+//                addresses and sizes, so each row's aligned covering block
+//                range is loaded, PcRing::pitch bytes apart; the producer
+//                funnel-shifts it into aligned 16-byte stores
+//                (symm::group_copy_ring_any) and the consumer copies head
+//                bytes, aligned vectors and tail bytes
+//                (symm::group_copy_tile_phase).  The covering range reads at
+//                most 15 bytes on either side of a row, inside the 16-byte
+//                granules of its first and last bytes.
+//
+// Discards: a slot is used for S blocks b, b + buffer_num, ... of its task;
+// after its last use its staging lines stay dirty in L2 (marked evict-last)
+// until they are written back, which costs DRAM bandwidth and, while they
+// wait, crowds the slots still in use out of L2.  With PcArgs::discard the
+// consumer release warp drops, after a slot's last use in the launch, every
+// 128-byte line that lies wholly inside the tile's rows (discard.global.L2),
+// before the release; lines shared with a neighbouring task's bytes are left
+// alone.  The CTA's last task is left out: nothing of this launch follows it
+// that its lines could crowd out, and discards there only delay the end of
+// the launch.  Discarding after every use instead measured slower (the
+// release waits for the discards, and the slot is rewritten while still in
+// L2).
 constexpr int kPcRelThreads = 320;
 #ifndef SYMM_PC_REL_LAG
 #define SYMM_PC_REL_LAG 4
 #endif
 constexpr int kPcRelLag = SYMM_PC_REL_LAG;  // done barriers per group (a power of two)
 static_assert((kPcRelLag & (kPcRelLag - 1)) == 0 && kPcRelLag >= 1, "lag: a power of two");
+// Ring entries of the release-warp kernel.
+#ifndef SYMM_PC_REL_PREFETCH
+#define SYMM_PC_REL_PREFETCH 2
+#endif
+constexpr int kPcRelPrefetch = SYMM_PC_REL_PREFETCH;
+// The instance for rows of any alignment (ANY = true) has its own ring depth,
+// consumer vectors in flight and residency: its producer shift-merges from
+// shared memory and its consumer copies byte edges, which need more
+// registers than 3 CTAs per SM leave.
+#ifndef SYMM_PC_ANY_RING
+#define SYMM_PC_ANY_RING 2
+#endif
+#ifndef SYMM_PC_ANY_CONSUMER_UNROLL
+#define SYMM_PC_ANY_CONSUMER_UNROLL 8
+#endif
+#ifndef SYMM_PC_ANY_MIN_BLOCKS
+#define SYMM_PC_ANY_MIN_BLOCKS 2
+#endif
+template <bool ANY>
+struct PcRelConf {
+  static constexpr int ring = ANY ? SYMM_PC_ANY_RING : kPcRelPrefetch;
+  static constexpr int min_blocks = ANY ? SYMM_PC_ANY_MIN_BLOCKS : kPcMinBlocks;
+  static constexpr int consumer_unroll = ANY ? SYMM_PC_ANY_CONSUMER_UNROLL : SYMM_PC_FLAT_UNROLL;
+  static_assert(kPcRelLag >= ring, "done barriers must outnumber ring entries");
+  static_assert((ring + 2 * kPcRelLag) * 8 <= 128, "barriers fit the ring's header");
+};
+// Before acquiring a slot, wait in shared memory until this CTA's other
+// group has released it (below).
+#ifndef SYMM_PC_LOCAL_WAIT
+#define SYMM_PC_LOCAL_WAIT 1
+#endif
+// Drop a slot's staging lines from L2 after its last use (PcArgs::discard).
+#ifndef SYMM_PC_DISCARD
+#define SYMM_PC_DISCARD 1
+#endif
+
+// The input ring of a2a_pc_rel_kernel.
+struct PcRing {
+  uint32_t stage;       // bytes per ring entry
+  uint32_t chunk_rows;  // tile rows per entry
+  uint32_t pitch;       // ANY: ring bytes per row (a multiple of 16)
+};
+
+__device__ __forceinline__ uint32_t pc_chunks(uint32_t rows, uint32_t chunk_rows) {
+  return (rows + chunk_rows - 1) / chunk_rows;
+}
+
+// Issues the bulk loads of rows r0 .. r0 + n - 1 of task k's input tile into
+// ring entry `buf` (one mbarrier phase): ANY, each row's 16-byte-aligned
+// covering block range, `pitch` bytes apart; otherwise the rows, packed.
+template <bool ANY>
+__device__ __forceinline__ void pc_prefetch_chunk(const PcArgs& a, const PcTask& k, uint32_t r0,
+                                                  uint32_t n, uint32_t pitch, uint8_t* buf,
+                                                  uint64_t* bar) {
+  const size_t src_row = (size_t)a.H * a.D * a.es;
+  const uint8_t* s0 = k.src + (size_t)r0 * src_row;
+  const uint64_t pol = symm::policy_evict_first();
+  if (!ANY) {
+    symm::mbar_arrive_expect_tx(bar, n * k.len);
+    for (uint32_t i = 0; i < n; ++i)
+      symm::bulk_load_hint(buf + i * k.len, s0 + i * src_row, k.len, bar, pol);
+    return;
+  }
+  const uintptr_t m16 = ~(uintptr_t)15;
+  uint32_t total = 0;
+  for (uint32_t i = 0; i < n; ++i) {
+    const uintptr_t s = (uintptr_t)(s0 + i * src_row);
+    total += (uint32_t)(((s + k.len + 15) & m16) - (s & m16));
+  }
+  symm::mbar_arrive_expect_tx(bar, total);
+  for (uint32_t i = 0; i < n; ++i) {
+    const uintptr_t s = (uintptr_t)(s0 + i * src_row);
+    const uintptr_t lo = s & m16;
+    symm::bulk_load_hint(buf + i * pitch, reinterpret_cast<const void*>(lo),
+                         (uint32_t)(((s + k.len + 15) & m16) - lo), bar, pol);
+  }
+}
 
 __device__ __forceinline__ uint64_t atom_exch_release(int64_t* p, int64_t v) {
   uint64_t old;
@@ -605,30 +750,35 @@ constexpr int kPcRelPW = SYMM_PC_REL_PRODUCER_WARPS;
 constexpr int kPcRelPG = 32 * kPcRelPW;        // producer group threads
 constexpr int kPcRelCG = 32 * (8 - kPcRelPW);  // consumer group threads
 
-__global__ void __launch_bounds__(kPcRelThreads, kPcMinBlocks)
-    a2a_pc_rel_kernel(const PcArgs a, uint32_t tile_bytes) {
+template <bool ANY>
+__global__ void __launch_bounds__(kPcRelThreads, PcRelConf<ANY>::min_blocks)
+    a2a_pc_rel_kernel(const PcArgs a, const PcRing rg) {
+  constexpr int kRing = PcRelConf<ANY>::ring;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int status[2];
+  // [role][parity of the group's barrier count]: thread 0 writes entry p
+  // again only after the group's next barrier, which every reader of the
+  // previous value has passed
+  __shared__ int status[2][2];
   __shared__ PcTable tab;
   __shared__ volatile uint32_t released[2];
-  static_assert((kPcPrefetch + 2 * kPcRelLag) * 8 <= 128, "barriers fit the ring's header");
-  uint64_t* in_full = reinterpret_cast<uint64_t*>(smem);  // kPcPrefetch ring barriers
-  uint64_t* done = in_full + kPcPrefetch;                  // [role][t % kPcRelLag]
+  uint64_t* in_full = reinterpret_cast<uint64_t*>(smem);  // kRing ring barriers
+  uint64_t* done = in_full + kRing;                        // [role][i % kPcRelLag]
   uint8_t* ring = smem + 128;
-  const int warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // 0 producer group, 1 consumer group, 2 release threads
   const int role = warp < kPcRelPW ? 0 : (warp < 8 ? 1 : 2);
   const int gtid = role == 0 ? (int)threadIdx.x : (int)threadIdx.x - kPcRelPG;
   const int gsize = role == 0 ? kPcRelPG : kPcRelCG;
   const int bar_id = 1 + role;
   const size_t stage_row = (size_t)a.H * a.W * a.D * a.es;
+  const size_t src_row = (size_t)a.H * a.D * a.es;
   const uint32_t nq = pc_tasks_per_cta(a);
   const uint64_t ntasks = (uint64_t)a.nbs * nq;
-  const uint64_t rotation = (uint64_t)nq * a.buffer_num;
-  const uint64_t lag = rotation < (uint64_t)kPcRelLag ? rotation : (uint64_t)kPcRelLag;
+  const uint64_t reuse = pc_slot_reuse(nq, a.buffer_num);
+  const uint64_t lag = reuse < (uint64_t)kPcRelLag ? reuse : (uint64_t)kPcRelLag;
   pc_table_fill(a, nq, tab);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kPcPrefetch; ++i) symm::mbar_init(&in_full[i], 1);
+    for (int i = 0; i < kRing; ++i) symm::mbar_init(&in_full[i], 1);
     for (int i = 0; i < kPcRelLag; ++i) {
       symm::mbar_init(&done[i], kPcRelPG);
       symm::mbar_init(&done[kPcRelLag + i], kPcRelCG);
@@ -645,78 +795,146 @@ __global__ void __launch_bounds__(kPcRelThreads, kPcMinBlocks)
 
   if (role < 2) {  // ------------------------------------ copy groups
     const uint64_t pol = symm::policy_evict_last();
+    const uint32_t msrc = (uint32_t)(src_row & 15);
     PcCursor cur;
-    for (uint64_t t = 0; t < ntasks; ++t, cur.next(nq, a.buffer_num)) {
+    uint64_t g = 0;  // barriers passed: chunks (producer) or tiles (consumer)
+    for (uint64_t t = 0; t < ntasks; ++t, cur.next(nq, a.nbs, a.buffer_num)) {
       const PcTask k = pc_task_at(a, tab, cur);
-      const int st = (int)(t % kPcPrefetch);
-      if (gtid == 0) {
-        int rc = symm::kSpinOk;
-        if (t + 1 > lag &&
-            !pc_count_wait(&released[role], (uint32_t)(t + 1 - lag), 2 * a.budget_ns, a.ctl))
-          rc = symm::kSpinTimeout;
-        if (rc == symm::kSpinOk && role == 0 &&
-            !pc_mbar_wait(&in_full[st], (uint32_t)(t / kPcPrefetch) & 1u, a.budget_ns, a.ctl)) {
-          symm::record_error(a.ctl, symm::kErrTimedOut, -1);
-          rc = symm::kSpinTimeout;
+      const uint32_t nch = role == 0 ? pc_chunks(k.rows, rg.chunk_rows) : 1;
+      for (uint32_t c = 0; c < nch; ++c, ++g) {
+        const int par = (int)(g & 1);
+        if (gtid == 0) {
+          int rc = symm::kSpinOk;
+          if (c == 0 && t + 1 > lag &&
+              !pc_count_wait(&released[role], (uint32_t)(t + 1 - lag), 2 * a.budget_ns, a.ctl))
+            rc = symm::kSpinTimeout;
+          if (rc == symm::kSpinOk && role == 0 &&
+              !pc_mbar_wait(&in_full[g % kRing], (uint32_t)(g / kRing) & 1u,
+                            a.budget_ns, a.ctl)) {
+            symm::record_error(a.ctl, symm::kErrTimedOut, -1);
+            rc = symm::kSpinTimeout;
+          }
+          if (rc == symm::kSpinOk && c == 0) {
+            // The slot's last holder is this CTA's other group: wait until
+            // its release is performed (the other role's count), so that the
+            // acquire finds the value at once instead of polling L2.
+            if (SYMM_PC_LOCAL_WAIT && role == 1 &&
+                !pc_count_wait(&released[0], (uint32_t)(t + 1), 2 * a.budget_ns, a.ctl))
+              rc = symm::kSpinTimeout;
+            if (SYMM_PC_LOCAL_WAIT && role == 0 && cur.b >= a.buffer_num &&
+                !pc_count_wait(&released[1], (uint32_t)(t + 1 - reuse), 2 * a.budget_ns, a.ctl))
+              rc = symm::kSpinTimeout;
+            if (rc == symm::kSpinOk)
+              rc = symm::spin_wait(k.slot, symm::kCmpEq, role == 0 ? 0 : 1, a.budget_ns, a.ctl,
+                                   a.err_base, a.err_bias);
+          }
+          status[role][par] = rc;
         }
-        if (rc == symm::kSpinOk)
-          rc = symm::spin_wait(k.slot, symm::kCmpEq, role == 0 ? 0 : 1, a.budget_ns, a.ctl,
-                               a.err_base, a.err_bias);
-        status[role] = rc;
-      }
-      symm::group_sync(bar_id, gsize);
-      if (status[role] != symm::kSpinOk) return;  // uniform across the group
-      if (role == 0) {
-        const uint8_t* tile = ring + (size_t)st * tile_bytes;
-        const uint32_t vrow = k.len >> 4, nv = k.rows * vrow;
-        const symm::TileStep step = symm::tile_step(kPcRelPG, vrow);
-        uint32_t i = (uint32_t)gtid / vrow, c = (uint32_t)gtid - i * vrow;
-        for (uint32_t v = gtid; v < nv; v += kPcRelPG, step.advance(i, c, vrow)) {
-          symm::st16_hint(k.stage + i * stage_row + 16 * c,
-                          *reinterpret_cast<const uint4*>(tile + i * k.len + 16 * c), pol);
+        symm::group_sync(bar_id, gsize);
+        if (status[role][par] != symm::kSpinOk) return;  // uniform across the group
+        if (role == 0) {
+          // ring entry -> rows r0 .. r0 + n - 1 of destination d's slot
+          const uint8_t* src = ring + (size_t)(g % kRing) * rg.stage;
+          const uint32_t r0 = c * rg.chunk_rows;
+          const uint32_t n = min(rg.chunk_rows, k.rows - r0);
+          uint8_t* dst = k.stage + (size_t)r0 * stage_row;
+          if (ANY) {
+            const uint32_t m0 = (uint32_t)((uintptr_t)(k.src + (size_t)r0 * src_row) & 15);
+            symm::group_copy_ring_any<kPcRelPG>(dst, (uint32_t)stage_row, src, rg.pitch, m0, msrc,
+                                                n, k.len, gtid, pol);
+          } else {
+            const uint32_t vrow = k.len >> 4, nv = n * vrow;
+            const symm::TileStep step = symm::tile_step(kPcRelPG, vrow);
+            uint32_t i = (uint32_t)gtid / vrow, cc = (uint32_t)gtid - i * vrow;
+            for (uint32_t v = gtid; v < nv; v += kPcRelPG, step.advance(i, cc, vrow))
+              symm::st16_hint(dst + i * stage_row + 16 * cc,
+                              *reinterpret_cast<const uint4*>(src + i * k.len + 16 * cc), pol);
+          }
+        } else if (ANY) {
+          symm::group_copy_tile_phase<kPcRelCG, PcRelConf<ANY>::consumer_unroll, symm::kCG, symm::kCS>(
+              k.dst, (uint32_t)stage_row, k.stage, (uint32_t)stage_row, k.rows, k.len, gtid);
+        } else {
+          symm::group_copy_tile<kPcRelCG, SYMM_PC_FLAT_UNROLL, symm::kCG, symm::kCS>(
+              k.dst, (uint32_t)stage_row, k.stage, (uint32_t)stage_row, k.rows, k.len >> 4, gtid);
         }
-      } else {
-        symm::group_copy_tile<kPcRelCG, SYMM_PC_FLAT_UNROLL, symm::kCG, symm::kCS>(
-            k.dst, (uint32_t)stage_row, k.stage, (uint32_t)stage_row, k.rows, k.len >> 4, gtid);
+        // this thread's copies precede the arrival
+        pc_mbar_arrive(&done[role * kPcRelLag + (g % kPcRelLag)]);
       }
-      pc_mbar_arrive(&done[role * kPcRelLag + (t % kPcRelLag)]);  // this thread's copies precede it
     }
   } else if (threadIdx.x == 256) {  // ---------------- producer release thread
-    uint64_t issued = 0;
-    PcCursor pre;
-    for (; issued < ntasks && issued < (uint64_t)kPcPrefetch; ++issued, pre.next(nq, a.buffer_num))
-      pc_prefetch(a, pc_task_at(a, tab, pre), ring + issued * tile_bytes, &in_full[issued]);
+    PcCursor pre;         // task of the next chunk to load
+    uint64_t pre_t = 0;   // its tile number
+    uint32_t pre_c = 0;   // the chunk within it
+    uint64_t issued = 0;  // chunks loaded, into ring entry issued % kRing
+    auto issue_next = [&]() {
+      if (pre_t >= ntasks) return;
+      const PcTask kp = pc_task_at(a, tab, pre);
+      const uint32_t r0 = pre_c * rg.chunk_rows;
+      const int e = (int)(issued % kRing);
+      symm::fence_proxy_async_shared();  // the group's reads of the entry precede the load
+      pc_prefetch_chunk<ANY>(a, kp, r0, min(rg.chunk_rows, kp.rows - r0), rg.pitch,
+                             ring + (size_t)e * rg.stage, &in_full[e]);
+      ++issued;
+      if (++pre_c == pc_chunks(kp.rows, rg.chunk_rows)) {
+        pre_c = 0;
+        ++pre_t;
+        pre.next(nq, a.nbs, a.buffer_num);
+      }
+    };
+    while (issued < (uint64_t)kRing && pre_t < ntasks) issue_next();
     PcCursor cur;
-    uint64_t t = 0;
-    for (; t < ntasks; ++t, cur.next(nq, a.buffer_num)) {
-      if (!pc_mbar_wait(&done[t % kPcRelLag], (uint32_t)(t / kPcRelLag) & 1u, 2 * a.budget_ns,
-                        a.ctl)) {
-        symm::record_error(a.ctl, symm::kErrTimedOut, -1);
-        break;
+    uint64_t g = 0;  // chunks done
+    bool ok = true;
+    for (uint64_t t = 0; ok && t < ntasks; ++t, cur.next(nq, a.nbs, a.buffer_num)) {
+      const PcTask k = pc_task_at(a, tab, cur);
+      const uint32_t nch = pc_chunks(k.rows, rg.chunk_rows);
+      for (uint32_t c = 0; c < nch; ++c, ++g) {
+        if (!pc_mbar_wait(&done[g % kPcRelLag], (uint32_t)(g / kPcRelLag) & 1u, 2 * a.budget_ns,
+                          a.ctl)) {
+          symm::record_error(a.ctl, symm::kErrTimedOut, -1);
+          ok = false;
+          break;
+        }
+        issue_next();  // chunk g's entry is free: the chunk kRing ahead
       }
-      if (issued < ntasks) {  // the group has read tile t's ring entry: refill it
-        symm::fence_proxy_async_shared();
-        pc_prefetch(a, pc_task_at(a, tab, pre), ring + (size_t)(t % kPcPrefetch) * tile_bytes,
-                    &in_full[t % kPcPrefetch]);
-        pre.next(nq, a.buffer_num);
-        ++issued;
-      }
-      const uint64_t old = atom_exch_release(pc_task_at(a, tab, cur).slot, 1);
+      if (!ok) break;
+      const uint64_t old = atom_exch_release(k.slot, 1);
       released[0] = (uint32_t)(t + 1) + zero_after(old);
     }
     // let the loads still in flight land before the CTA may leave (bounded)
-    for (uint64_t i = t; i < issued; ++i)
-      symm::mbar_wait(&in_full[i % kPcPrefetch], (uint32_t)(i / kPcPrefetch) & 1u, a.budget_ns);
-  } else if (threadIdx.x == 288) {  // ---------------- consumer release thread
+    for (uint64_t i = g; i < issued; ++i)
+      symm::mbar_wait(&in_full[i % kRing], (uint32_t)(i / kRing) & 1u,
+                      a.budget_ns);
+  } else if (warp == 9) {  // ------------------------ consumer release warp
     PcCursor cur;
-    for (uint64_t t = 0; t < ntasks; ++t, cur.next(nq, a.buffer_num)) {
-      if (!pc_mbar_wait(&done[kPcRelLag + (t % kPcRelLag)], (uint32_t)(t / kPcRelLag) & 1u,
-                        2 * a.budget_ns, a.ctl)) {
-        symm::record_error(a.ctl, symm::kErrTimedOut, -1);
+    for (uint64_t t = 0; t < ntasks; ++t, cur.next(nq, a.nbs, a.buffer_num)) {
+      int ok = 1;
+      if (lane == 0)
+        ok = pc_mbar_wait(&done[kPcRelLag + (t % kPcRelLag)], (uint32_t)(t / kPcRelLag) & 1u,
+                          2 * a.budget_ns, a.ctl);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();  // lane 0's acquire of the group's copies precedes every lane's discards
+      if (!ok) {
+        if (lane == 0) symm::record_error(a.ctl, symm::kErrTimedOut, -1);
         break;
       }
-      const uint64_t old = atom_exch_release(pc_task_at(a, tab, cur).slot, 0);
-      released[1] = (uint32_t)(t + 1) + zero_after(old);
+      const PcTask k = pc_task_at(a, tab, cur);
+      if (a.discard && cur.b + a.buffer_num >= a.nbs && (!SYMM_PC_TASK_MAJOR || cur.j + 1 < nq)) {
+        // the slot's last use, with more of the CTA's tasks to come: every
+        // 128-byte line wholly inside one of the tile's staging rows
+        for (uint32_t i = 0; i < k.rows; ++i) {
+          const uintptr_t row = (uintptr_t)(k.stage + (size_t)i * stage_row);
+          const uintptr_t hi = (row + k.len) & ~(uintptr_t)127;
+          for (uintptr_t x = ((row + 127) & ~(uintptr_t)127) + 128 * (uintptr_t)lane; x < hi;
+               x += 128 * 32)
+            symm::discard_l2(reinterpret_cast<const void*>(x));
+        }
+        __syncwarp();  // every lane's discards precede the release
+      }
+      if (lane == 0) {
+        const uint64_t old = atom_exch_release(k.slot, 0);
+        released[1] = (uint32_t)(t + 1) + zero_after(old);
+      }
     }
   }
 }
@@ -904,6 +1122,7 @@ int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
   a.nbs = (p.S + p.tile_s - 1) / p.tile_s;
   a.buffer_num = p.buffer_num;
   a.reset = p.reset ? 1u : 0u;
+  a.discard = SYMM_PC_DISCARD ? 1u : 0u;
   a.tile_src = (size_t)p.tile_s * p.H * p.D * p.es;
   a.tile_dst = (size_t)p.tile_s * p.H * p.W * p.D * p.es;
   a.stage_buf = a.tile_dst;
@@ -927,15 +1146,26 @@ int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
                                          : kCopyRows;
   const size_t tile_bytes = (size_t)p.tile_s * bd * p.es;
   const size_t tasks = (size_t)p.W * p.W * p.H * nbd;
+  const size_t row_max = (size_t)std::min(bd, (uint32_t)p.D) * p.es;  // bytes of a full D block
   const void* kfn;
   int threads;
   size_t smem, smem_limit;
+  PcRing rg{0, 0, 0};
+  bool rel = false;
   {
     // input prefetch by bulk copies (one per tile row) when every tile row is
     // 16-byte aligned and at least kPcMinPrefetchRow bytes, and a tile fits
     // the shared-memory ring; narrower rows are copied faster by the group
     const bool prefetch = !p.vector_only && mode == kCopyAligned &&
-                          (size_t)bd * p.es >= kPcMinPrefetchRow && tile_bytes <= kPcMaxPrefetchTile;
+                          row_max >= kPcMinPrefetchRow && tile_bytes <= kPcMaxPrefetchTile;
+    // rows of any alignment: prefetch of their covering block ranges, in
+    // chunks of rows, when staging and output rows share one 16-byte phase
+    const size_t any_pitch = (row_max + 30) & ~(size_t)15;
+    const bool prefetch_any = SYMM_PC_ANY_PREFETCH && SYMM_PC_RELEASE_WARPS && !p.vector_only &&
+                              mode == kCopyAny && row_max >= kPcMinPrefetchRowAny &&
+                              any_pitch <= kPcMaxPrefetchTile &&
+                              (uintptr_t)p.out % 16 == (uintptr_t)p.staging % 16 &&
+                              p.slab % 16 == 0 && p.stage_pe % 16 == 0;
     kfn = prefetch                  ? (const void*)a2a_pc_kernel<true, kCopyAligned>
           : mode == kCopyAligned    ? (const void*)a2a_pc_kernel<false, kCopyAligned>
           : mode == kCopyAny        ? (const void*)a2a_pc_kernel<false, kCopyAny>
@@ -944,8 +1174,23 @@ int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
     smem = prefetch ? 128 + (size_t)kPcPrefetch * tile_bytes : 0;
     smem_limit = prefetch ? 128 + (size_t)kPcPrefetch * kPcMaxPrefetchTile : 0;
     if (prefetch && SYMM_PC_RELEASE_WARPS) {
-      kfn = (const void*)a2a_pc_rel_kernel;
+      rg.chunk_rows = (uint32_t)p.tile_s;  // a whole tile per ring entry
+      rg.pitch = (uint32_t)row_max;
+      rg.stage = (uint32_t)tile_bytes;
+      kfn = (const void*)a2a_pc_rel_kernel<false>;
+      rel = true;
+    } else if (prefetch_any) {
+      rg.pitch = (uint32_t)any_pitch;
+      rg.chunk_rows = (uint32_t)std::min((size_t)p.tile_s, kPcMaxPrefetchTile / any_pitch);
+      rg.stage = rg.chunk_rows * rg.pitch;
+      kfn = (const void*)a2a_pc_rel_kernel<true>;
+      rel = true;
+    }
+    if (rel) {
+      const size_t ring = prefetch ? PcRelConf<false>::ring : PcRelConf<true>::ring;
       threads = kPcRelThreads;
+      smem = 128 + ring * rg.stage;
+      smem_limit = 128 + ring * kPcMaxPrefetchTile;
     }
   }
   // tasks of one S block, dealt evenly: k per CTA, ceil(tasks / k) CTAs,
@@ -956,8 +1201,10 @@ int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
   const size_t per_cta = (tasks + cap - 1) / cap;
   const int grid = (int)((tasks + per_cta - 1) / per_cta);
   uint32_t tb = (uint32_t)tile_bytes;
-  void* args[] = {&a, &tb};
-  return cuda_check(cudaLaunchKernel(kfn, dim3((unsigned)grid), dim3(threads), args, smem, s),
+  void* args_pc[] = {&a, &tb};
+  void* args_rel[] = {&a, &rg};
+  return cuda_check(cudaLaunchKernel(kfn, dim3((unsigned)grid), dim3(threads),
+                                     rel ? args_rel : args_pc, smem, s),
                     (std::string(what) + ": PC launch").c_str());
 }
 

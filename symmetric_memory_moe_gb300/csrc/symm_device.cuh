@@ -371,6 +371,89 @@ __device__ __forceinline__ void group_copy_tile_any(uint8_t* dst, uint32_t dst_r
     }
 }
 
+// Head and tail bytes of a tile whose rows all have the same head (bytes
+// before dst's next 16-byte boundary), nvec body vectors and tail; source
+// byte x of row i at src_of(i) + x, read with load kind LK (kRO or kCG), or
+// plainly when LK < 0 (shared memory).  One byte per thread-step.
+template <int G, int LK, typename SrcOf>
+__device__ __forceinline__ void group_copy_edges(uint8_t* dst, uint32_t dst_row, SrcOf src_of,
+                                                 uint32_t rows, uint32_t head, uint32_t nvec,
+                                                 uint32_t tail, int gtid) {
+  const uint32_t edge = head + tail;  // at most 15 + 15
+  if (!edge) return;
+  for (uint32_t e = gtid; e < rows * 32; e += G) {
+    const uint32_t i = e >> 5, k = e & 31;
+    if (k >= edge) continue;
+    const uint32_t x = k < head ? k : head + (nvec << 4) + (k - head);
+    const uint8_t* s = src_of(i) + x;
+    if constexpr (LK < 0)
+      st1(dst + i * dst_row + x, *s);
+    else
+      st1(dst + i * dst_row + x, ld1<LK>(s));
+  }
+}
+
+// A tile of rows x len bytes whose source and destination rows share one
+// 16-byte phase ((dst - src) % 16 == 0, both row strides multiples of 16),
+// at any alignment: byte heads and tails, and a body of aligned 16-byte
+// vectors copied with the whole tile flattened over the group
+// (group_copy_tile).
+template <int G, int U, int LK, int SK>
+__device__ __forceinline__ void group_copy_tile_phase(uint8_t* dst, uint32_t dst_row,
+                                                      const uint8_t* src, uint32_t src_row,
+                                                      uint32_t rows, uint32_t len, int gtid) {
+  uint32_t head = (uint32_t)((16 - ((uintptr_t)dst & 15)) & 15);
+  if (head > len) head = len;
+  const uint32_t nvec = (len - head) >> 4;
+  const uint32_t tail = len - head - (nvec << 4);
+  group_copy_tile<G, U, LK, SK>(dst + head, dst_row, src + head, src_row, rows, nvec, gtid);
+  group_copy_edges<G, LK>(
+      dst, dst_row, [&](uint32_t i) { return src + i * src_row; }, rows, head, nvec, tail, gtid);
+}
+
+// Rows of len bytes from a shared-memory ring to global memory, any
+// alignment.  Ring row i (pitch bytes apart, 16-byte aligned) holds the
+// 16-byte-aligned block range covering source row i, whose first byte sits
+// at ring offset m_i = (m0 + i * msrc) % 16 (the source rows' addresses mod
+// 16 step by msrc).  Destination rows are dst_row bytes apart, dst_row a
+// multiple of 16, so they share one head, nvec body vectors and one tail.  A
+// body vector is the funnel shift of the two aligned ring blocks under it;
+// stores carry the L2 policy `pol`.  A warp copies a row, its lanes taking
+// the row's vectors in turn (shared-memory loads are short, so one in
+// flight per lane suffices).
+template <int G>
+__device__ __forceinline__ void group_copy_ring_any(uint8_t* dst, uint32_t dst_row,
+                                                    const uint8_t* ring, uint32_t pitch,
+                                                    uint32_t m0, uint32_t msrc, uint32_t rows,
+                                                    uint32_t len, int gtid, uint64_t pol) {
+  uint32_t head = (uint32_t)((16 - ((uintptr_t)dst & 15)) & 15);
+  if (head > len) head = len;
+  const uint32_t nvec = (len - head) >> 4;
+  const uint32_t tail = len - head - (nvec << 4);
+  // a warp per row, its lanes along the row
+  for (uint32_t i = (uint32_t)gtid >> 5; i < rows; i += G / 32) {
+    const uint32_t q0 = ((m0 + i * msrc) & 15) + head;  // ring byte of the row's first vector
+    const uint8_t* rrow = ring + i * pitch;
+    uint8_t* drow = dst + i * dst_row + head;
+    for (uint32_t c = gtid & 31; c < nvec; c += 32) {
+      const uint32_t q = q0 + 16 * c;
+      const uint8_t* p = rrow + (q & ~15u);
+      uint4 x = *reinterpret_cast<const uint4*>(p);
+      if (q & 15) x = funnel16(x, *reinterpret_cast<const uint4*>(p + 16), q & 15);
+      st16_hint(drow + 16 * c, x, pol);
+    }
+  }
+  group_copy_edges<G, -1>(
+      dst, dst_row, [&](uint32_t i) { return ring + i * pitch + ((m0 + i * msrc) & 15); }, rows,
+      head, nvec, tail, gtid);
+}
+
+// Drops the 128-byte L2 line at p (128-byte aligned) without writing it
+// back: its contents become undefined.
+__device__ __forceinline__ void discard_l2(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // ------------------------------------------------------- warp byte copy ---
 // One warp copies n bytes src -> dst (any alignments, non-overlapping).
 //  * head: bytes up to dst's next 16-byte boundary, one byte per lane;

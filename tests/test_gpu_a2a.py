@@ -230,6 +230,25 @@ def test_pc_any_alignment_tiles(W, S, H, D, es, shift):
         assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
 
 
+@pytest.mark.parametrize("W,S,H,D,es,tile_s,block_d,buf,shift", [
+    (4, 19, 2, 999, 2, 32, 600, 2, 6),    # D blocks of 1200 and 798 bytes; chunks of 16 + 3 rows
+    (4, 37, 4, 1501, 1, 40, 0, 1, 3),     # odd 1501-byte rows, one buffer; chunks of 21 + 16 rows
+    (2, 50, 8, 1099, 2, 16, 0, 3, 13),    # 2198-byte rows, 3 buffers; chunks of 14 + 2 rows
+    (16, 5, 1, 601, 2, 3, 0, 2, 1),       # 1202-byte rows, many tasks per CTA
+])
+def test_pc_any_prefetch(W, S, H, D, es, tile_s, block_d, buf, shift):
+    """Rows of 1 KB and more that are not 16-byte aligned, with staging and
+    output rows in one 16-byte phase: the producer's input arrives by bulk
+    copies of each row's aligned covering range, in chunks of rows (a tile
+    taller than a ring entry takes several), and is shift-merged from shared
+    memory.  Ragged S and D blocks, one to three buffers, input shifted so
+    that the rows' source phases differ from the destination's (each input
+    object ends at least 13 bytes before its 256-byte granule does)."""
+    xe = _rand_bytes(W, S * W, H, D, es, seed=D * 3 + shift).reshape(W, S * W, H, D, es)
+    got = _run_es(xe, W, S, H, D, es, "pc", tile_s, block_d, buf, shift, 0)
+    assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
+
+
 @pytest.mark.parametrize("W,S,H,buf,tile_s", [
     (2, 24, 1, 1, 4),    # one slot per CTA, one buffer: reused by the very next tile
     (2, 24, 1, 2, 4),    # two slots in rotation
