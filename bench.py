@@ -44,6 +44,8 @@ WORKLOAD = "dsv3"
 # buffers (a 38.5 MB staging ring; measured best of 3-64 rows, 512-2048
 # columns, 1-6 buffers)
 PC_TILE_S, PC_BLOCK_D, PC_BUFFERS = 14, 1024, 3
+# the tail shape's producer/consumer tiles are the workload's 32 rows; buffers measured best
+TAIL_PC_BUFFERS = 3
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 L2_BYTES = 126 * 2**20  # smaller than the part's L2: data this size stays resident
 
@@ -498,17 +500,19 @@ def time_variants(args, peak):
     # tail: W32 S256 H2 D999 fp16 (1998-byte rows), direct and P/C with 32-row tiles
     W, S, H, D, es = 32, 256, 2, 999, 2
     for variant in ("direct", "pc"):
-        b = CombineBuffers(W, S * W, H, D, es, pc=variant == "pc", S=S, tile_s=32)
+        b = CombineBuffers(W, S * W, H, D, es, pc=variant == "pc", S=S, tile_s=32,
+                           buffer_num=TAIL_PC_BUFFERS)
         _fill_random(b.heap, b.inp, b.nbytes, 4)
         kind = abi.SYMM_A2A_PC if variant == "pc" else abi.SYMM_A2A_DIRECT
 
         def call(b=b, kind=kind):
-            abi.all2all_combine(b.heap.handle, b.inp, b.out, W, S, H, D, es, kind, 32, 0, 2,
-                                b.staging, b.signals)
+            abi.all2all_combine(b.heap.handle, b.inp, b.out, W, S, H, D, es, kind, 32, 0,
+                                TAIL_PC_BUFFERS, b.staging, b.signals)
         ms = _time_calls(call, steps, args.warmup, graph=False)
         _check_runs(b.heap, b.inp, b.out, W, S, H * D * es)
         record(f"tail_{variant}", "combine tail: W=32 S=256 H=2 D=999 fp16", 2 * W * b.nbytes,
-               ms, "launches", {"tile_s": 32} if variant == "pc" else None)
+               ms, "launches",
+               {"tile_s": 32, "buffer_num": TAIL_PC_BUFFERS} if variant == "pc" else None)
         done(b.heap)
     # the two-phase combine on the DeepSeek-V3 shape (tiles of 64 x 1024)
     W, S, H, D, es = 8, 2048, 1, 7168, 2

@@ -413,6 +413,12 @@ constexpr size_t kPcMinPrefetchRow = 2048;
 #define SYMM_PC_ANY_PREFETCH 1
 #endif
 constexpr size_t kPcMinPrefetchRowAny = 1024;
+// Bytes of input rows per ring entry of the unaligned instance (at most
+// kPcMaxPrefetchTile; a row wider than this takes an entry of its own).
+#ifndef SYMM_PC_ANY_CHUNK
+#define SYMM_PC_ANY_CHUNK 32768
+#endif
+constexpr uint32_t kPcAnyChunk = SYMM_PC_ANY_CHUNK;
 
 // How a group copies its tile (a tile always spans less than 4 GiB here):
 //   kCopyAligned  every tile row, base and row stride is 16-byte aligned:
@@ -554,10 +560,17 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
 //              kPcRelLag that alternate);
 //   warps 4-7  consumer group: thread 0 acquires (== 1), the group copies the
 //              staged tile out and arrives on the tile's done barrier;
+//   (a slot's last holder is always this CTA's other group, so thread 0
+//   first waits for that group's release count in shared memory -- the
+//   release is then performed in L2 -- and acquires with a single load
+//   instead of polling L2; the producer group also starts tile t only once
+//   the consumer group has released tile t - R, R as below, when tile t's
+//   slot is fresh (a task's first S blocks): a CTA's staged tiles not yet
+//   consumed then never exceed R, which bounds what L2 must hold);
 //   warp 8     producer release thread: per chunk, waits for its done
 //              barrier and refills its ring entry with the next input chunk;
-//              after a tile's last chunk, releases the slot (1) and counts it
-//              in released[0];
+//              after a tile's last chunk, releases the slot (1), counts it in
+//              released[0], and only then refills that chunk's entry;
 //   warp 9     consumer release warp: per tile, waits for done[1], drops the
 //              staging lines of a slot's last use from L2 when
 //              PcArgs::discard is set (below), releases (0) and counts it
@@ -569,9 +582,9 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
 // the group waits for from its last use, and the done barrier of tile
 // t - kPcRelLag (the same one of the kPcRelLag that alternate) has been
 // consumed.  The producer group reuses a
-// done barrier per chunk; it is never more than kPcRelPrefetch chunks ahead
-// of its release thread (a chunk's ring entry is refilled only after the
-// chunk kPcRelPrefetch earlier is done), so kPcRelLag >= kPcRelPrefetch
+// done barrier per chunk; it is never more than a ring's worth of chunks
+// ahead of its release thread (a chunk's ring entry is refilled only after
+// the chunk one ring earlier is done), so kPcRelLag >= the ring's entries
 // keeps those phases apart too.  The release is an atomic exchange whose
 // result the count depends on, so the count moves only once the release is
 // performed in L2, where the group's acquire reads.  Waits on another role's
@@ -629,6 +642,11 @@ constexpr int kPcRelPrefetch = SYMM_PC_REL_PREFETCH;
 #ifndef SYMM_PC_ANY_CONSUMER_UNROLL
 #define SYMM_PC_ANY_CONSUMER_UNROLL 8
 #endif
+// 16-byte vectors in flight per lane in the producer's shift-merge copy
+// out of the ring (symm::group_copy_ring_any).
+#ifndef SYMM_PC_RING_UNROLL
+#define SYMM_PC_RING_UNROLL 1
+#endif
 #ifndef SYMM_PC_ANY_MIN_BLOCKS
 #define SYMM_PC_ANY_MIN_BLOCKS 2
 #endif
@@ -640,11 +658,6 @@ struct PcRelConf {
   static_assert(kPcRelLag >= ring, "done barriers must outnumber ring entries");
   static_assert((ring + 2 * kPcRelLag) * 8 <= 128, "barriers fit the ring's header");
 };
-// Before acquiring a slot, wait in shared memory until this CTA's other
-// group has released it (below).
-#ifndef SYMM_PC_LOCAL_WAIT
-#define SYMM_PC_LOCAL_WAIT 1
-#endif
 // Drop a slot's staging lines from L2 after its last use (PcArgs::discard).
 #ifndef SYMM_PC_DISCARD
 #define SYMM_PC_DISCARD 1
@@ -818,10 +831,11 @@ __global__ void __launch_bounds__(kPcRelThreads, PcRelConf<ANY>::min_blocks)
             // The slot's last holder is this CTA's other group: wait until
             // its release is performed (the other role's count), so that the
             // acquire finds the value at once instead of polling L2.
-            if (SYMM_PC_LOCAL_WAIT && role == 1 &&
+            if (role == 1 &&
                 !pc_count_wait(&released[0], (uint32_t)(t + 1), 2 * a.budget_ns, a.ctl))
               rc = symm::kSpinTimeout;
-            if (SYMM_PC_LOCAL_WAIT && role == 0 && cur.b >= a.buffer_num &&
+            // (pacing: also when tile t's slot is fresh, see above)
+            if (role == 0 && t >= reuse &&
                 !pc_count_wait(&released[1], (uint32_t)(t + 1 - reuse), 2 * a.budget_ns, a.ctl))
               rc = symm::kSpinTimeout;
             if (rc == symm::kSpinOk)
@@ -840,8 +854,8 @@ __global__ void __launch_bounds__(kPcRelThreads, PcRelConf<ANY>::min_blocks)
           uint8_t* dst = k.stage + (size_t)r0 * stage_row;
           if (ANY) {
             const uint32_t m0 = (uint32_t)((uintptr_t)(k.src + (size_t)r0 * src_row) & 15);
-            symm::group_copy_ring_any<kPcRelPG>(dst, (uint32_t)stage_row, src, rg.pitch, m0, msrc,
-                                                n, k.len, gtid, pol);
+            symm::group_copy_ring_any<kPcRelPG, SYMM_PC_RING_UNROLL>(
+                dst, (uint32_t)stage_row, src, rg.pitch, m0, msrc, n, k.len, gtid, pol);
           } else {
             const uint32_t vrow = k.len >> 4, nv = n * vrow;
             const symm::TileStep step = symm::tile_step(kPcRelPG, vrow);
@@ -895,11 +909,16 @@ __global__ void __launch_bounds__(kPcRelThreads, PcRelConf<ANY>::min_blocks)
           ok = false;
           break;
         }
-        issue_next();  // chunk g's entry is free: the chunk kRing ahead
+        // chunk g's entry is free: load the chunk kRing ahead into it, after
+        // the release and its count when this is the tile's last chunk (both
+        // are on the slot's cycle; measured faster than refilling first, or
+        // refilling while the release is in flight)
+        if (c + 1 < nch) issue_next();
       }
       if (!ok) break;
       const uint64_t old = atom_exch_release(k.slot, 1);
       released[0] = (uint32_t)(t + 1) + zero_after(old);
+      issue_next();
     }
     // let the loads still in flight land before the CTA may leave (bounded)
     for (uint64_t i = g; i < issued; ++i)
@@ -1181,7 +1200,8 @@ int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
       rel = true;
     } else if (prefetch_any) {
       rg.pitch = (uint32_t)any_pitch;
-      rg.chunk_rows = (uint32_t)std::min((size_t)p.tile_s, kPcMaxPrefetchTile / any_pitch);
+      rg.chunk_rows = (uint32_t)std::min(
+          (size_t)p.tile_s, std::max((size_t)1, (size_t)kPcAnyChunk / any_pitch));
       rg.stage = rg.chunk_rows * rg.pitch;
       kfn = (const void*)a2a_pc_rel_kernel<true>;
       rel = true;

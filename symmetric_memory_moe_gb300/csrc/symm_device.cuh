@@ -419,9 +419,8 @@ __device__ __forceinline__ void group_copy_tile_phase(uint8_t* dst, uint32_t dst
 // multiple of 16, so they share one head, nvec body vectors and one tail.  A
 // body vector is the funnel shift of the two aligned ring blocks under it;
 // stores carry the L2 policy `pol`.  A warp copies a row, its lanes taking
-// the row's vectors in turn (shared-memory loads are short, so one in
-// flight per lane suffices).
-template <int G>
+// the row's vectors in turn, U at a time.
+template <int G, int U>
 __device__ __forceinline__ void group_copy_ring_any(uint8_t* dst, uint32_t dst_row,
                                                     const uint8_t* ring, uint32_t pitch,
                                                     uint32_t m0, uint32_t msrc, uint32_t rows,
@@ -430,17 +429,25 @@ __device__ __forceinline__ void group_copy_ring_any(uint8_t* dst, uint32_t dst_r
   if (head > len) head = len;
   const uint32_t nvec = (len - head) >> 4;
   const uint32_t tail = len - head - (nvec << 4);
-  // a warp per row, its lanes along the row
+  // a warp per row, its lanes along the row, U vectors in flight per lane
   for (uint32_t i = (uint32_t)gtid >> 5; i < rows; i += G / 32) {
     const uint32_t q0 = ((m0 + i * msrc) & 15) + head;  // ring byte of the row's first vector
     const uint8_t* rrow = ring + i * pitch;
     uint8_t* drow = dst + i * dst_row + head;
-    for (uint32_t c = gtid & 31; c < nvec; c += 32) {
-      const uint32_t q = q0 + 16 * c;
-      const uint8_t* p = rrow + (q & ~15u);
-      uint4 x = *reinterpret_cast<const uint4*>(p);
-      if (q & 15) x = funnel16(x, *reinterpret_cast<const uint4*>(p + 16), q & 15);
-      st16_hint(drow + 16 * c, x, pol);
+    for (uint32_t c0 = gtid & 31; c0 < nvec; c0 += 32 * U) {
+      uint4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t q = q0 + 16 * (c0 + 32 * u);
+        const uint8_t* p = rrow + (q & ~15u);
+        if (c0 + 32 * u < nvec) {
+          x[u] = *reinterpret_cast<const uint4*>(p);
+          if (q & 15) x[u] = funnel16(x[u], *reinterpret_cast<const uint4*>(p + 16), q & 15);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (c0 + 32 * u < nvec) st16_hint(drow + 16 * (c0 + 32 * u), x[u], pol);
     }
   }
   group_copy_edges<G, -1>(

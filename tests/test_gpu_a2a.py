@@ -234,7 +234,10 @@ def test_pc_any_alignment_tiles(W, S, H, D, es, shift):
     (4, 19, 2, 999, 2, 32, 600, 2, 6),    # D blocks of 1200 and 798 bytes; chunks of 16 + 3 rows
     (4, 37, 4, 1501, 1, 40, 0, 1, 3),     # odd 1501-byte rows, one buffer; chunks of 21 + 16 rows
     (2, 50, 8, 1099, 2, 16, 0, 3, 13),    # 2198-byte rows, 3 buffers; chunks of 14 + 2 rows
-    (16, 5, 1, 601, 2, 3, 0, 2, 1),       # 1202-byte rows, many tasks per CTA
+    (16, 5, 1, 601, 2, 3, 0, 2, 1),       # 1202-byte rows
+    (32, 9, 2, 999, 2, 2, 0, 1, 5),       # 2048 tasks per S block: several per CTA, one buffer
+    (32, 9, 2, 999, 2, 2, 0, 3, 5),       # the same with 3 buffers (slots fresh for 3 S blocks)
+    (32, 9, 3, 1101, 2, 2, 550, 2, 3),    # 9216 tasks: more per CTA than the task table holds
 ])
 def test_pc_any_prefetch(W, S, H, D, es, tile_s, block_d, buf, shift):
     """Rows of 1 KB and more that are not 16-byte aligned, with staging and
@@ -243,7 +246,10 @@ def test_pc_any_prefetch(W, S, H, D, es, tile_s, block_d, buf, shift):
     taller than a ring entry takes several), and is shift-merged from shared
     memory.  Ragged S and D blocks, one to three buffers, input shifted so
     that the rows' source phases differ from the destination's (each input
-    object ends at least 13 bytes before its 256-byte granule does)."""
+    object ends at least 13 bytes before its 256-byte granule does).  With
+    W = 32 each CTA owns several tasks and walks them one after another:
+    the producer is paced on its own consumer across task boundaries, and a
+    slot's staging lines are dropped from L2 after its last use."""
     xe = _rand_bytes(W, S * W, H, D, es, seed=D * 3 + shift).reshape(W, S * W, H, D, es)
     got = _run_es(xe, W, S, H, D, es, "pc", tile_s, block_d, buf, shift, 0)
     assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
