@@ -295,13 +295,13 @@ def oracle_rate(o, xb, wl, rows: int, min_s: float, max_runs: int = 50):
 
 
 def cpu_baseline(wl, min_s: float = 8.0) -> dict:
-    """The oracle on the machine's host cores: its OpenMP build (the combine's loop
-    over the W destinations split across threads) and the plain build on one
-    thread, each on a token sample for about min_s seconds."""
+    """The oracle on the machine's host cores: its OpenMP build (the combine's loops
+    over the destinations and rows split across nproc threads) and the plain
+    build on one thread, each on a token sample for about min_s seconds."""
     import oracle
 
     nproc = os.cpu_count() or 1
-    threads = min(nproc, wl.W)  # the parallel loop has W iterations
+    threads = nproc  # the parallel loops have W x rows iterations
     rows = 512
     xb = _oracle_sample(wl, rows)
     one, sec1, runs1, moved = oracle_rate(oracle.load(), xb, wl, rows, min_s)
@@ -319,7 +319,7 @@ def cpu_baseline(wl, min_s: float = 8.0) -> dict:
     line.update({"value": round(many, 4), "cores": threads,
                  "sample": f"oracle combine on W={wl.W} S={rows} H={wl.H} D={wl.D} bf16 ({rows}/"
                            f"{wl.S} of the tokens, {moved / 1e9:.3f} GB moved): its OpenMP build "
-                           f"over the {wl.W} destinations on {threads} threads, median of {runsn} "
+                           f"over (destination, row) on {threads} threads, median of {runsn} "
                            f"runs ({secn:.2f} s each); the plain build on one thread, median of "
                            f"{runs1} runs ({sec1:.2f} s each)",
                  "single_thread": {"value": round(one, 4), "unit": UNIT, "cores": 1}})
@@ -336,10 +336,10 @@ def run_reference(args):
 
     wl = inputs.WORKLOADS[WORKLOAD]
     nproc = os.cpu_count() or 1
-    threads = min(nproc, wl.W)
+    threads = nproc
     os.environ["OMP_NUM_THREADS"] = str(threads)
     try:
-        o, kind = oracle.load_openmp(), f"OpenMP build over the {wl.W} destinations, " \
+        o, kind = oracle.load_openmp(), f"OpenMP build over (destination, row), " \
                                         f"{threads} threads"
     except Exception:
         o, kind, threads = oracle.load(), "plain build, one thread", 1

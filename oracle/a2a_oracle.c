@@ -33,10 +33,11 @@ int oracle_combine(const void *in, void *out, int64_t W, int64_t S, int64_t H,
     if (W < 1 || S < 0 || H < 0 || D < 0 || es < 1) return -1;
     const unsigned char *src = (const unsigned char *)in;
     unsigned char *dst = (unsigned char *)out;
-    /* Each d writes only out_d: the OpenMP build (timed CPU baseline only)
-     * splits the loop over d across threads; the plain build ignores this. */
+    /* Each (d, s) writes only row s of out_d: the OpenMP build (timed CPU
+     * baseline only) splits the loops over d and s across threads; the plain
+     * build ignores this. */
 #ifdef _OPENMP
-#pragma omp parallel for schedule(static)
+#pragma omp parallel for collapse(2) schedule(static)
 #endif
     for (int64_t d = 0; d < W; d++)
         for (int64_t s = 0; s < S; s++)

@@ -21,8 +21,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "a2a_oracle.c")
 BUILD_DIR = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liba2a_oracle.so")
-# the same source built with -fopenmp: oracle_combine splits its loop over the
-# destination rank d across threads.  Only the timed CPU baseline uses it.
+# the same source built with -fopenmp: oracle_combine splits its loops over the
+# destination rank d and the row s across threads.  Only the timed CPU
+# baseline uses it.
 OMP_LIB_PATH = os.path.join(BUILD_DIR, "liba2a_oracle_omp.so")
 
 
@@ -247,8 +248,8 @@ def load(path: str | None = None) -> Oracle:
 
 
 def load_openmp() -> Oracle:
-    """The oracle built with -fopenmp (its combine runs over d in parallel,
-    OMP_NUM_THREADS threads), for the timed CPU baseline."""
+    """The oracle built with -fopenmp (its combine runs over (d, s) in
+    parallel, OMP_NUM_THREADS threads), for the timed CPU baseline."""
     return Oracle(build(out=OMP_LIB_PATH, openmp=True))
 
 

@@ -2,7 +2,8 @@
 from the committed ncu figures only while the kernel sources still hash to
 the captured ones, and it is the slope of two captures of different sizes
 (DRAM bytes per algorithmic byte) times the launch's algorithmic bytes; the
-reference arm reports the same workload config as the GPU arm."""
+reference arm reports the same workload config as the GPU arm; the oracle's
+OpenMP build that the CPU baseline times computes what the plain build does."""
 import json
 import os
 import shutil
@@ -52,3 +53,17 @@ def test_both_arms_report_one_config():
         assert c == bench.bench_config(1, variant)
         assert (c["W"], c["S"], c["H"], c["D"]) == (8, 2048, 1, 7168)
         assert c["bytes_per_step"] == 2 * 8 * 2048 * 8 * 7168 * 2
+
+
+def test_openmp_oracle_build_matches_the_plain_build(monkeypatch):
+    """The CPU baseline times the oracle's OpenMP build (its loops over
+    destination and row split across threads): it must compute the same
+    combine as the plain build, also with more threads than destinations."""
+    import numpy as np
+
+    import oracle
+
+    monkeypatch.setenv("OMP_NUM_THREADS", "5")
+    x = np.random.default_rng(3).integers(-2**15, 2**15, (4, 4 * 13, 3, 7), dtype=np.int16)
+    want = oracle.load().combine(x, 4, 13, 3, 7)
+    assert np.array_equal(oracle.load_openmp().combine(x, 4, 13, 3, 7), want)
