@@ -43,7 +43,7 @@ WORKLOAD = "dsv3"
 # producer/consumer tiling of the DeepSeek-V3 step: 14 x 1024 tiles, 3
 # buffers (a 38.5 MB staging ring; measured best of 3-64 rows, 512-2048
 # columns, 1-6 buffers)
-PC_TILE_S, PC_BLOCK_D, PC_BUFFERS = 14, 1024, 3
+PC_TILE_S, PC_BLOCK_D, PC_BUFFERS = 12, 1024, 3
 # the tail shape's producer/consumer tiles are the workload's 32 rows; buffers measured best
 TAIL_PC_BUFFERS = 3
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
