@@ -464,20 +464,24 @@ def time_variants(args, peak):
         out[name] = e
 
     steps = max(args.steps, 10)
-    # small: W8 S128 H8 D128 bf16 (16.8 MB in, L2-resident), direct and P/C
+    # small: W8 S128 H8 D128 bf16 (16.8 MB in, L2-resident), direct and P/C;
+    # P/C with one 128-row tile per task and one buffer, measured fastest on
+    # this shape (every handshake costs more than pipelining S blocks saves)
     W, S, H, D, es = 8, 128, 8, 128, 2
-    for variant, tile in (("direct", 0), ("pc", 64)):
-        b = CombineBuffers(W, S * W, H, D, es, pc=variant == "pc", S=S, tile_s=tile or 16)
+    for variant, tile, nbuf in (("direct", 0, 2), ("pc", 128, 1)):
+        b = CombineBuffers(W, S * W, H, D, es, pc=variant == "pc", S=S, tile_s=tile or 16,
+                           buffer_num=nbuf)
         _fill_random(b.heap, b.inp, b.nbytes, 1)
         kind = abi.SYMM_A2A_PC if variant == "pc" else abi.SYMM_A2A_DIRECT
 
-        def call(b=b, kind=kind, tile=tile):
+        def call(b=b, kind=kind, tile=tile, nbuf=nbuf):
             abi.all2all_combine(b.heap.handle, b.inp, b.out, W, S, H, D, es, kind, tile or 16, 0,
-                                2, b.staging, b.signals)
+                                nbuf, b.staging, b.signals)
         ms = _time_calls(call, steps, args.warmup, graph=True)
         _check_runs(b.heap, b.inp, b.out, W, S, H * D * es)
         record(f"small_{variant}", "combine small: W=8 S=128 H=8 D=128 bf16", 2 * W * b.nbytes,
-               ms, "CUDA graph of 20 calls", {"tile_s": tile} if tile else None)
+               ms, "CUDA graph of 20 calls",
+               {"tile_s": tile, "buffer_num": nbuf} if tile else None)
         done(b.heap)
     # round trip: W16 S1024 H4 D128 fp16, dispatch then its inverse
     W, S, H, D, es = 16, 1024, 4, 128, 2
