@@ -39,7 +39,9 @@ def _worker(rank, world, port, out):
 
 def test_max_over_two_gloo_ranks():
     world = 2
-    out = mp.Manager().dict()
+    # the manager process is spawned too: this test process may already run
+    # threads (the OpenMP oracle), and a fork from a threaded process can hang
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert dict(out) == {0: 4.5, 1: 4.5}
 
