@@ -40,9 +40,9 @@ METRIC = "reverse-All2All combine GB/s (read+write) and % of GB300 HBM roofline"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = "dsv3"
-# producer/consumer tiling of the DeepSeek-V3 step: 14 x 1024 tiles, 3
-# buffers (a 38.5 MB staging ring; measured best of 3-64 rows, 512-2048
-# columns, 1-6 buffers)
+# producer/consumer tiling of the DeepSeek-V3 step: 12 x 1024 tiles, 3
+# buffers (a 33 MB staging ring; measured best of 6-24 rows, 512-2048
+# columns, 2-4 buffers)
 PC_TILE_S, PC_BLOCK_D, PC_BUFFERS = 12, 1024, 3
 # the tail shape's producer/consumer tiles are the workload's 32 rows; buffers measured best
 TAIL_PC_BUFFERS = 3
