@@ -20,10 +20,11 @@
 //    group, each synchronised by its own named barrier.  The grid is capped at
 //    the CTAs that are resident at once, so every spin can be satisfied.
 //  * A task (destination d, source r, expert h, D block) is one signal slot;
-//    like the page's cores, each CTA owns a fixed set of tasks and walks the
-//    S blocks in order, its consumer group consuming exactly the tiles its own
-//    producer group staged.  Every wait is thus satisfied by the same CTA,
-//    and successive producers of a slot are ordered.  The page's target
+//    like the page's cores, each CTA owns a fixed set of tasks and walks each
+//    task's S blocks in order (task by task, where the page's cores go S
+//    block by S block), its consumer group consuming exactly the tiles its
+//    own producer group staged.  Every wait is thus satisfied by the same
+//    CTA, and successive producers of a slot are ordered.  The page's target
 //    rotation (rank + i) % W staggers one PE's producers across
 //    destinations; here every (r, d) pair is in flight at once, so it has
 //    nothing left to stagger.
@@ -61,7 +62,7 @@ namespace {
 #define SYMM_RUNS_MIN_BLOCKS 2
 #endif
 #ifndef SYMM_RUNS_GENERAL_UNROLL
-#define SYMM_RUNS_GENERAL_UNROLL 2
+#define SYMM_RUNS_GENERAL_UNROLL 3
 #endif
 #ifndef SYMM_RUNS_GENERAL_MIN_BLOCKS
 #define SYMM_RUNS_GENERAL_MIN_BLOCKS 6
@@ -581,11 +582,11 @@ __global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
 // block by S block): the slot of tile t - R then no longer holds the value
 // the group waits for from its last use, and the done barrier of tile
 // t - kPcRelLag (the same one of the kPcRelLag that alternate) has been
-// consumed.  The producer group reuses a
-// done barrier per chunk; it is never more than a ring's worth of chunks
-// ahead of its release thread (a chunk's ring entry is refilled only after
-// the chunk one ring earlier is done), so kPcRelLag >= the ring's entries
-// keeps those phases apart too.  The release is an atomic exchange whose
+// consumed.  The producer group arrives on a done barrier per chunk; it is
+// never more than a ring's worth of chunks ahead of its release thread (a
+// chunk's ring entry is refilled only after the chunk one ring earlier is
+// done), so kPcRelLag >= the ring's entries keeps those phases apart too.
+// The release is an atomic exchange whose
 // result the count depends on, so the count moves only once the release is
 // performed in L2, where the group's acquire reads.  Waits on another role's
 // progress (a release thread on its group, a group on its release thread)
@@ -627,7 +628,7 @@ constexpr int kPcRelThreads = 320;
 #endif
 constexpr int kPcRelLag = SYMM_PC_REL_LAG;  // done barriers per group (a power of two)
 static_assert((kPcRelLag & (kPcRelLag - 1)) == 0 && kPcRelLag >= 1, "lag: a power of two");
-// Ring entries of the release-warp kernel.
+// Ring entries of the release-warp kernel's instance for aligned rows.
 #ifndef SYMM_PC_REL_PREFETCH
 #define SYMM_PC_REL_PREFETCH 2
 #endif
