@@ -127,6 +127,73 @@ __global__ void __launch_bounds__(kRunThreads,
   }
 }
 
+// --------------------------------------------------- direct, short runs ---
+// The same permutation for runs of at most kBatchMaxVec 16-byte vectors
+// (16-byte aligned): one warp per run would keep only a few vectors in
+// flight per lane and pay a whole memory round trip per run.  Consecutive
+// runs of a period are linear in one index -- the source PE r for the
+// combine and dispatch (period W: run k = (d*Sb + s)*W + r, sources in_pe
+// apart, destinations R apart), the row s for the inverse (period Sb: run
+// k = (r*W + d)*Sb + s, sources W*R apart, destinations R apart) -- so a
+// warp copies a batch of m of them as one tile of m rows, kBatchUnroll
+// vectors in flight per lane.  Batches never cross a period.
+#ifndef SYMM_RUNS_BATCH_UNROLL
+#define SYMM_RUNS_BATCH_UNROLL 8
+#endif
+#ifndef SYMM_RUNS_BATCH_MIN_BLOCKS
+#define SYMM_RUNS_BATCH_MIN_BLOCKS 4
+#endif
+constexpr int kBatchUnroll = SYMM_RUNS_BATCH_UNROLL;
+constexpr uint32_t kBatchMaxVec = 256;  // runs of at most 4 KB take the batches
+template <bool INVERSE>
+__global__ void __launch_bounds__(kRunThreads, SYMM_RUNS_BATCH_MIN_BLOCKS)
+    a2a_runs_batch_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, size_t in_pe,
+                          size_t out_pe, uint32_t W, uint32_t Sb, uint32_t R, uint32_t nruns,
+                          uint32_t m) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t warp = (blockIdx.x * kRunThreads + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * kRunThreads) >> 5;
+  const uint32_t P = INVERSE ? Sb : W;  // runs per period
+  const uint32_t nbp = (P + m - 1) / m;  // batches per period
+  const uint32_t nbatch = nruns / P * nbp;
+  const uint32_t nvec = R >> 4;
+  const symm::TileStep step = symm::tile_step(32, nvec);
+  const uint32_t i0 = (uint32_t)lane / nvec, c0 = (uint32_t)lane - i0 * nvec;
+  for (uint32_t bi = warp; bi < nbatch; bi += nwarps) {
+    const uint32_t pi = bi / nbp, j0 = (bi - pi * nbp) * m;  // period, its first run
+    const uint32_t rows = min(m, P - j0);
+    const uint8_t* src;
+    uint8_t* dst;
+    size_t sstride;
+    if (!INVERSE) {
+      const uint32_t s = pi % Sb, d = pi / Sb;
+      src = in + j0 * in_pe + (size_t)(d * Sb + s) * R;
+      dst = out + d * out_pe + (size_t)(s * W + j0) * R;
+      sstride = in_pe;
+    } else {
+      const uint32_t d = pi % W, r = pi / W;
+      src = in + d * in_pe + (size_t)(j0 * W + r) * R;
+      dst = out + r * out_pe + (size_t)(d * Sb + j0) * R;
+      sstride = (size_t)W * R;
+    }
+    const uint32_t nv = rows * nvec;
+    uint32_t i = i0, c = c0;
+    for (uint32_t v0 = 0; v0 < nv; v0 += 32 * kBatchUnroll) {
+      uint4 x[kBatchUnroll];
+      uint32_t doff[kBatchUnroll];
+#pragma unroll
+      for (int u = 0; u < kBatchUnroll; ++u) {
+        doff[u] = i * R + 16 * c;
+        if (v0 + 32 * u + lane < nv) x[u] = symm::ld16_ro(src + i * sstride + 16 * c);
+        step.advance(i, c, nvec);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatchUnroll; ++u)
+        if (v0 + 32 * u + lane < nv) symm::st16_cs(dst + doff[u], x[u]);
+    }
+  }
+}
+
 // ------------------------------------------------------ direct, bulk ---
 // The same run permutation moved by the Tensor Memory Accelerator: one thread
 // per CTA streams units (runs cut into <= kBulkChunk-byte pieces) through a
@@ -1074,6 +1141,26 @@ int symm_host::launch_runs_raw(const uint8_t* in, uint8_t* out, size_t in_pe, si
   if (nruns > 0x7fffffffull) return fail(SYMM_EINVAL, std::string(what) + ": more than 2^31 runs");
   const bool aligned = R % 16 == 0 && (uintptr_t)in % 16 == 0 && (uintptr_t)out % 16 == 0 &&
                        in_pe % 16 == 0 && out_pe % 16 == 0;
+  const uint32_t period = inverse ? Sb : W;
+  if (aligned && R <= 16 * kBatchMaxVec && period >= 2) {
+    // short runs: batches of m runs per warp, about two rounds of vectors each
+    const uint32_t nvec = (uint32_t)(R >> 4);
+    const uint32_t m = std::min(period, std::max(2u, (uint32_t)(64 * kBatchUnroll) / nvec));
+    const void* bfn = inverse ? (const void*)a2a_runs_batch_kernel<true>
+                              : (const void*)a2a_runs_batch_kernel<false>;
+    int bcap = resident_ctas(bfn, kRunThreads);
+    if (bcap <= 0) bcap = 4 * (sm_count() > 0 ? sm_count() : 1);
+    const size_t nbatch = nruns / period * ((period + m - 1) / m);
+    const size_t bneed = (nbatch + kRunThreads / 32 - 1) / (kRunThreads / 32);
+    const int bgrid = (int)(bneed < (size_t)bcap ? bneed : (size_t)bcap);
+    if (inverse)
+      a2a_runs_batch_kernel<true><<<bgrid, kRunThreads, 0, s>>>(in, out, in_pe, out_pe, W, Sb,
+                                                                (uint32_t)R, (uint32_t)nruns, m);
+    else
+      a2a_runs_batch_kernel<false><<<bgrid, kRunThreads, 0, s>>>(in, out, in_pe, out_pe, W, Sb,
+                                                                 (uint32_t)R, (uint32_t)nruns, m);
+    return cuda_check(cudaGetLastError(), what);
+  }
   const void* kfn = inverse ? (aligned ? (const void*)a2a_runs_kernel<true, true>
                                        : (const void*)a2a_runs_kernel<true, false>)
                             : (aligned ? (const void*)a2a_runs_kernel<false, true>

@@ -137,6 +137,47 @@ def _rand_bytes(W, rows, H, D, es, seed):
     return torch.randint(0, 256, (W, rows, H, D * es), generator=g, dtype=torch.uint8)
 
 
+@pytest.mark.parametrize("op,W,S,H,D", [
+    ("combine", 3, 5, 1, 8),         # 16-byte runs: one batch holds a whole period (3 runs)
+    ("combine", 5, 3, 1, 2048),      # 4 KB runs: batches of 2, the last of a period holds 1
+    ("combine", 7, 4, 1, 520),       # 1040-byte runs: batches of 7
+    ("combine", 1, 6, 2, 64),        # one PE: a period of 1 run, the per-run kernel
+    ("combine", 4, 3, 1, 2056),      # 4112-byte runs: past the batches, the per-run kernel
+    ("dispatch", 6, 12, 3, 16),      # 96-byte runs, S' = 2
+    ("combine_back", 4, 9, 1, 1024), # inverse, period S' = 9 in batches of 4, 4, 1
+    ("combine_back", 3, 1, 2, 32),   # inverse with S' = 1: the per-run kernel
+])
+def test_short_run_batches(op, W, S, H, D):
+    """Aligned runs of at most 4 KB are copied in batches of consecutive runs
+    per warp (a period: the W source PEs of one output row for the combine
+    and dispatch, the S' rows of one (PE, PE) pair for the inverse); batches
+    end with the period.  S is the combine's S, dispatch's S or the inverse's
+    S'.  Bit-exact against the oracle, on bf16-sized elements."""
+    es = 2
+    rows_in = {"combine": S * W, "dispatch": S, "combine_back": S * W}[op]
+    xe = _rand_bytes(W, rows_in, H, D, es, seed=W * 100 + S + D)
+    n = rows_in * H * D * es
+    bufs = CombineBuffers(W, rows_in, H, D, es, extra=256)
+    heap = bufs.heap
+    heap.upload(bufs.inp, xe.reshape(W, -1))
+    heap.views(bufs.out, n).fill_(POISON)
+    xv = np.ascontiguousarray(xe.numpy()).view(np.dtype((np.void, es)))
+    o = oracle.load()
+    if op == "combine":
+        abi.all2all_combine(heap.handle, bufs.inp, bufs.out, W, S, H, D, es, abi.SYMM_A2A_DIRECT,
+                            16, 0, 2, 0, 0)
+        want = o.combine(xv.reshape(W, S * W, H, D), W, S, H, D)
+    elif op == "dispatch":
+        abi.all2all_dispatch(heap.handle, bufs.inp, bufs.out, W, S, H, D, es)
+        want = o.dispatch(xv.reshape(W, S, H, D), W, S, H, D)
+    else:
+        abi.all2all_combine_back(heap.handle, bufs.inp, bufs.out, W, S, H, D, es)
+        want = o.combine_back(xv.reshape(W, S, H * W, D), W, S, H, D)
+    torch.cuda.synchronize()
+    assert_bits_equal(heap.download(bufs.out, n), want.view(np.uint8).reshape(W, -1))
+    heap.close()
+
+
 @pytest.mark.parametrize("W,S,H,D,es,tile_s,block_d,buf", [
     (1, 7, 3, 5, 2, 4, 0, 2),        # one PE: identity
     (3, 37, 2, 999, 2, 16, 256, 2),   # odd W, ragged S and D blocks
