@@ -67,6 +67,16 @@ extern "C" {
  * shared memory where every run is 16-byte aligned. */
 #define SYMM_A2A_FLAG_VECTOR 0x200
 #define SYMM_A2A_FLAG_BULK 0x400
+/* OR-ed into SYMM_A2A_PC, for debugging: a barrier between producers and
+ * consumers.  Each S block runs as two launches -- every producer stages its
+ * tile and releases its slot, then every consumer acquires, copies out and
+ * returns its slot -- so no consumer overlaps any producer ([RA2A] "MTE
+ * Implementation" with a global barrier per S block in place of the
+ * pipelining).  Same staging, slots and results, far slower: a result that
+ * is right with this flag and wrong without it points at the
+ * synchronisation rather than at the index arithmetic.  Slots are always
+ * zeroed first (SYMM_A2A_FLAG_NO_RESET is ignored). */
+#define SYMM_A2A_FLAG_PHASED 0x800
 
 /* bytes at the start of every slab that the heap keeps for itself */
 #define SYMM_HEAP_HEADER_BYTES 4096

@@ -30,6 +30,7 @@ SYMM_A2A_PC = 1
 SYMM_A2A_FLAG_NO_RESET = 0x100
 SYMM_A2A_FLAG_VECTOR = 0x200
 SYMM_A2A_FLAG_BULK = 0x400
+SYMM_A2A_FLAG_PHASED = 0x800
 SYMM_HEAP_HEADER_BYTES = 4096
 SYMM_SIGNAL_STRIDE_BYTES = 64
 SYMM_NOALLOC_SCRATCH_BYTES = 32 << 20

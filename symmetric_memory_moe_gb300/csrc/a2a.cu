@@ -1026,6 +1026,47 @@ __global__ void __launch_bounds__(kPcRelThreads, PcRelConf<ANY>::min_blocks)
   }
 }
 
+// ------------------------------------- producer / consumer, phased ---
+// SYMM_A2A_FLAG_PHASED (a debugging aid): the producers of one S block, or
+// its consumers, as one launch of one CTA per task whose warps take the
+// tile's rows.  Kernel boundaries stand in for a barrier between the two
+// roles; the slot protocol is the pipelined kernels' (producer: wait 0,
+// copy, release 1; consumer: wait 1, copy, release 0), so a slot's waits
+// are satisfied as soon as they start.
+constexpr int kPcPhaseThreads = 256;
+template <int ROLE>  // 0: producers, 1: consumers
+__global__ void __launch_bounds__(kPcPhaseThreads) a2a_pc_phase_kernel(const PcArgs a, uint32_t b) {
+  __shared__ int status;
+  const PcTask k = pc_task_of(a, pc_base(a, blockIdx.x), b, b % a.buffer_num);
+  if (threadIdx.x == 0)
+    status = symm::spin_wait(k.slot, symm::kCmpEq, ROLE == 0 ? 0 : 1, a.budget_ns, a.ctl,
+                             a.err_base, a.err_bias);
+  __syncthreads();
+  if (status != symm::kSpinOk) return;  // uniform across the CTA
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t stage_row = (size_t)a.H * a.W * a.D * a.es;
+  const size_t src_row = (size_t)a.H * a.D * a.es;
+  for (uint32_t i = warp; i < k.rows; i += kPcPhaseThreads / 32) {
+    if (ROLE == 0)
+      symm::warp_copy<4, symm::kRO, symm::kST>(k.stage + i * stage_row, k.src + i * src_row,
+                                               k.len, lane);
+    else
+      symm::warp_copy<4, symm::kCG, symm::kCS>(k.dst + i * stage_row, k.stage + i * stage_row,
+                                               k.len, lane);
+  }
+  __syncthreads();  // the CTA's copies precede the release
+  if (threadIdx.x == 0) symm::st_release(k.slot, ROLE == 0 ? 1 : 0);
+}
+// Every signal slot of every PE to 0 (before a phased call).
+__global__ void pc_phase_zero_kernel(const PcArgs a) {
+  const size_t per_pe = (size_t)a.buffer_num * a.W * a.nbd * a.H;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < per_pe * a.W;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t d = i / per_pe, j = i - d * per_pe;
+    *reinterpret_cast<int64_t*>(a.signals + d * a.sig_pe + j * SYMM_SIGNAL_STRIDE_BYTES) = 0;
+  }
+}
+
 // ------------------------------------------------------------ launching ---
 // CTAs of `kernel` (launched with `threads` threads and `smem` bytes of
 // dynamic shared memory) that are resident on the current device at once;
@@ -1205,11 +1246,12 @@ extern "C" int all2all_pc_workspace(int W, int S, int H, int D, int elem_bytes, 
 }
 
 // Zeroes, picks the instance for and launches one producer/consumer combine.
-int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
+namespace {
+// The kernels' arguments for a plan; false when a tile row exceeds 4 GiB.
+bool make_pc_args(const PcPlan& p, PcArgs* out) {
   const uint32_t bd = p.block_d ? (uint32_t)p.block_d : (uint32_t)p.D;
   const uint32_t nbd = (p.D + bd - 1) / bd;
-  if ((uint64_t)std::min(bd, (uint32_t)p.D) * p.es > 0xffffffffull)
-    return fail(SYMM_EINVAL, std::string(what) + ": a tile row (block_d * elem_bytes) exceeds 4 GiB");
+  if ((uint64_t)std::min(bd, (uint32_t)p.D) * p.es > 0xffffffffull) return false;
   PcArgs a;
   a.in = p.in;
   a.out = p.out;
@@ -1238,6 +1280,36 @@ int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
   a.ctl = static_cast<Control*>(p.ctl);
   a.err_base = p.err_base;
   a.err_bias = p.err_bias;
+  *out = a;
+  return true;
+}
+
+// SYMM_A2A_FLAG_PHASED: zero every slot, then per S block one launch of all
+// producers and one of all consumers (see a2a_pc_phase_kernel).
+int launch_pc_phased(const PcPlan& p, cudaStream_t s, const char* what) {
+  PcArgs a;
+  if (!make_pc_args(p, &a))
+    return fail(SYMM_EINVAL, std::string(what) + ": a tile row (block_d * elem_bytes) exceeds 4 GiB");
+  const size_t tasks = (size_t)a.W * a.W * a.H * a.nbd;
+  if (tasks > 0x7fffffffull) return fail(SYMM_EINVAL, std::string(what) + ": too many tasks");
+  const size_t slots = tasks * a.buffer_num;
+  pc_phase_zero_kernel<<<(unsigned)std::min<size_t>((slots + 255) / 256, 1024), 256, 0, s>>>(a);
+  int rc = cuda_check(cudaGetLastError(), what);
+  for (uint32_t b = 0; rc == SYMM_OK && b < a.nbs; ++b) {
+    a2a_pc_phase_kernel<0><<<(unsigned)tasks, kPcPhaseThreads, 0, s>>>(a, b);
+    a2a_pc_phase_kernel<1><<<(unsigned)tasks, kPcPhaseThreads, 0, s>>>(a, b);
+    rc = cuda_check(cudaGetLastError(), what);
+  }
+  return rc;
+}
+}  // namespace
+
+int symm_host::launch_pc(const PcPlan& p, cudaStream_t s, const char* what) {
+  PcArgs a;
+  if (!make_pc_args(p, &a))
+    return fail(SYMM_EINVAL, std::string(what) + ": a tile row (block_d * elem_bytes) exceeds 4 GiB");
+  const uint32_t bd = a.block_d;
+  const uint32_t nbd = a.nbd;
   // every tile row, base and row stride 16-byte aligned
   const bool aligned = ((size_t)p.D * p.es) % 16 == 0 && ((size_t)bd * p.es) % 16 == 0 &&
                        (uintptr_t)p.in % 16 == 0 && (uintptr_t)p.out % 16 == 0 &&
@@ -1359,6 +1431,7 @@ static int combine_pc(symm_heap* h, size_t in_off, size_t out_off, size_t nbytes
   p.ctl = h->base;
   p.err_base = h->base;
   p.err_bias = 0;
+  if (flags & SYMM_A2A_FLAG_PHASED) return launch_pc_phased(p, s, "all2all_combine");
   return launch_pc(p, s, "all2all_combine");
 }
 
@@ -1371,7 +1444,8 @@ extern "C" int all2all_combine(symm_heap_t* h, const void* in, void* out, int W,
                       &out_off, &nbytes);
   if (rc) return rc;
   const int kind = variant & 0xff, flags = variant & ~0xff;
-  if (flags & ~(SYMM_A2A_FLAG_NO_RESET | SYMM_A2A_FLAG_VECTOR | SYMM_A2A_FLAG_BULK))
+  if (flags &
+      ~(SYMM_A2A_FLAG_NO_RESET | SYMM_A2A_FLAG_VECTOR | SYMM_A2A_FLAG_BULK | SYMM_A2A_FLAG_PHASED))
     return fail(SYMM_EINVAL, "all2all_combine: unknown flag");
   cudaStream_t s = as_stream(stream);
   if (kind == SYMM_A2A_DIRECT)

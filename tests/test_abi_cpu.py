@@ -28,6 +28,25 @@ def test_header_declares_the_boundary():
         assert must in names
 
 
+def test_binding_constants_match_the_header():
+    """Every integer SYMM_* constant the binding defines has the header's
+    value (codes, enums, flags, sizes)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    defines = {}
+    for name, value in re.findall(r"^#define\s+(SYMM_\w+)\s+(.+?)\s*$", text, flags=re.M):
+        try:
+            # drop C integer suffixes (32u, 1ll) before evaluating the expression
+            expr = re.sub(r"\b(\d+)(?:[uU]?[lL]{0,2}|[lL]{1,2}[uU])\b", r"\1", value)
+            defines[name] = int(eval(expr, {}))
+        except Exception:
+            continue
+    shared = [n for n in dir(abi) if n.startswith("SYMM_") and isinstance(getattr(abi, n), int)]
+    assert len(shared) > 10
+    for name in shared:
+        assert name in defines, f"{name} is not #defined in the header"
+        assert getattr(abi, name) == defines[name], name
+
+
 def test_library_exports_every_declared_symbol():
     path = build.build()
     out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,

@@ -296,6 +296,35 @@ def test_pc_any_prefetch(W, S, H, D, es, tile_s, block_d, buf, shift):
     assert_bits_equal(got, _expect_es(xe, W, S, H, D, es))
 
 
+@pytest.mark.parametrize("W,S,H,D,es,tile_s,block_d,buf,shift", [
+    (4, 19, 2, 999, 2, 32, 600, 2, 6),   # unaligned rows, ragged S and D blocks
+    (8, 40, 1, 1024, 2, 12, 0, 3, 0),    # 2 KB rows, 3 buffers
+    (3, 10, 2, 7, 3, 4, 0, 1, 0),        # 3-byte elements, one buffer
+])
+def test_pc_phased_mode(W, S, H, D, es, tile_s, block_d, buf, shift):
+    """SYMM_A2A_FLAG_PHASED, the debugging mode in which each S block's
+    producers and then its consumers run as separate launches (a barrier
+    between the roles): the oracle's result, every slot back at 0, also when
+    the slots held stale values before the call (the mode zeroes them)."""
+    xe = _rand_bytes(W, S * W, H, D, es, seed=D + tile_s + buf).reshape(W, S * W, H, D, es)
+    bufs = CombineBuffers(W, S * W, H, D, es, pc=True, S=S, tile_s=tile_s, block_d=block_d,
+                          buffer_num=buf, extra=2048)
+    heap, n = bufs.heap, bufs.nbytes
+    inp = bufs.inp + shift
+    heap.upload(inp, xe.reshape(W, -1))
+    heap.views(bufs.out, n).fill_(POISON)
+    heap.views(bufs.signals, bufs.signal_bytes).fill_(0x7F)
+    abi.all2all_combine(heap.handle, inp, bufs.out, W, S, H, D, es,
+                        abi.SYMM_A2A_PC | abi.SYMM_A2A_FLAG_PHASED, tile_s, block_d, buf,
+                        bufs.staging, bufs.signals)
+    torch.cuda.synchronize()
+    assert abi.symm_check_error(heap.handle)[0] == abi.SYMM_OK
+    assert_bits_equal(heap.download(bufs.out, n), _expect_es(xe, W, S, H, D, es))
+    sig = heap.download(bufs.signals, bufs.signal_bytes).view(torch.int64)[:, ::8]
+    assert not sig.any()
+    heap.close()
+
+
 @pytest.mark.parametrize("W,S,H,buf,tile_s", [
     (2, 24, 1, 1, 4),    # one slot per CTA, one buffer: reused by the very next tile
     (2, 24, 1, 2, 4),    # two slots in rotation
