@@ -194,6 +194,110 @@ __global__ void __launch_bounds__(kRunThreads, SYMM_RUNS_BATCH_MIN_BLOCKS)
   }
 }
 
+// ----------------------------------------------- direct, unaligned runs ---
+// Runs that are not 16-byte aligned, of kRingMinRun bytes up to a slot: the
+// general instance above keeps only a few vectors in flight in registers
+// and is bound by memory latency.  Here each warp streams its runs through
+// its own ring of kRingSlots shared-memory slots: lane 0 loads the 16-byte-
+// aligned block range covering a run with one bulk (TMA) copy (at most 15
+// bytes on either side of the run, inside the granules of its first and last
+// bytes), completing on the slot's mbarrier; the warp then funnel-shifts the
+// slot into aligned 16-byte stores (byte heads and tails) and lane 0 reloads
+// the slot with the run kRingSlots ahead.  Device memory only.  Warps take
+// runs grid-stride in the order of a2a_runs_kernel.
+#ifndef SYMM_RUNS_RING
+#define SYMM_RUNS_RING 1
+#endif
+constexpr int kRingWarps = 8;
+constexpr int kRingSlots = 3;
+constexpr uint32_t kRingMinRun = 1024;
+constexpr uint32_t kRingMaxSlot = 8192;
+constexpr uint32_t kRingHeader = 256;  // kRingWarps x kRingSlots mbarriers
+static_assert(kRingWarps * kRingSlots * 8 <= kRingHeader, "ring barriers fit the header");
+template <bool INVERSE>
+__global__ void __launch_bounds__(32 * kRingWarps)
+    a2a_runs_ring_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, size_t in_pe,
+                         size_t out_pe, uint32_t W, uint32_t Sb, uint32_t R, uint32_t nruns,
+                         uint32_t slot_bytes, uint64_t budget_ns, Control* ctl) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem) + wib * kRingSlots;
+  uint8_t* ring = smem + kRingHeader + (size_t)wib * kRingSlots * slot_bytes;
+  const uint32_t warp = blockIdx.x * kRingWarps + wib;
+  const uint32_t nwarps = gridDim.x * kRingWarps;
+  auto run_at = [&](uint32_t k, const uint8_t** src, uint8_t** dst) {
+    if (!INVERSE) {
+      const uint32_t r = k % W, t = k / W, s = t % Sb, d = t / Sb;
+      *src = in + r * in_pe + (size_t)(d * Sb + s) * R;
+      *dst = out + d * out_pe + (size_t)(s * W + r) * R;
+    } else {
+      const uint32_t s = k % Sb, t = k / Sb, d = t % W, r = t / W;
+      *src = in + d * in_pe + (size_t)(s * W + r) * R;
+      *dst = out + r * out_pe + (size_t)(d * Sb + s) * R;
+    }
+  };
+  auto load = [&](uint32_t k, int slot) {  // lane 0: run k's covering range into `slot`
+    const uint8_t* src;
+    uint8_t* dst;
+    run_at(k, &src, &dst);
+    const uintptr_t lo = (uintptr_t)src & ~(uintptr_t)15;
+    const uint32_t n = (uint32_t)((((uintptr_t)src + R + 15) & ~(uintptr_t)15) - lo);
+    symm::mbar_arrive_expect_tx(&full[slot], n);
+    symm::bulk_load(ring + (size_t)slot * slot_bytes, reinterpret_cast<const void*>(lo), n,
+                    &full[slot]);
+  };
+  if (lane == 0) {
+    for (int i = 0; i < kRingSlots; ++i) symm::mbar_init(&full[i], 1);
+    symm::fence_mbar_init();
+    for (int i = 0; i < kRingSlots; ++i)
+      if (warp + (uint64_t)i * nwarps < nruns) load(warp + i * nwarps, i);
+  }
+  __syncwarp();
+  uint32_t it = 0;
+  for (uint32_t k = warp; k < nruns; k += nwarps, ++it) {
+    const int slot = (int)(it % kRingSlots);
+    int ok = 1;
+    if (lane == 0) ok = symm::mbar_wait(&full[slot], (it / kRingSlots) & 1u, budget_ns);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();  // lane 0 saw the slot land; the others read it after this
+    if (!ok) {
+      if (lane == 0) {
+        symm::record_error(ctl, symm::kErrTimedOut, -1);
+        // let this warp's loads still in flight land before it leaves (bounded)
+        for (uint32_t j = 0; j < (uint32_t)kRingSlots && k + (uint64_t)j * nwarps < nruns; ++j)
+          symm::mbar_wait(&full[(it + j) % kRingSlots], ((it + j) / kRingSlots) & 1u, budget_ns);
+      }
+      return;  // uniform across the warp
+    }
+    symm::mbar_try_wait(&full[slot], (it / kRingSlots) & 1u);  // every lane observes the phase
+    const uint8_t* src;
+    uint8_t* dst;
+    run_at(k, &src, &dst);
+    const uint8_t* sl = ring + (size_t)slot * slot_bytes;
+    const uint32_t m = (uint32_t)((uintptr_t)src & 15);  // the run's first byte in the slot
+    uint32_t head = (uint32_t)((16 - ((uintptr_t)dst & 15)) & 15);
+    if (head > R) head = R;
+    const uint32_t nvec = (R - head) >> 4, tail = R - head - (nvec << 4);
+    for (uint32_t c = lane; c < nvec; c += 32) {
+      const uint32_t q = m + head + 16 * c;
+      const uint8_t* p = sl + (q & ~15u);
+      uint4 x = *reinterpret_cast<const uint4*>(p);
+      if (q & 15) x = symm::funnel16(x, *reinterpret_cast<const uint4*>(p + 16), q & 15);
+      symm::st16_cs(dst + head + 16 * c, x);
+    }
+    if ((uint32_t)lane < head) symm::st1(dst + lane, sl[m + lane]);
+    if ((uint32_t)lane < tail) {
+      const uint32_t x = head + (nvec << 4) + lane;
+      symm::st1(dst + x, sl[m + x]);
+    }
+    __syncwarp();  // every lane has read the slot
+    if (lane == 0 && k + (uint64_t)kRingSlots * nwarps < nruns) {
+      symm::fence_proxy_async_shared();  // those reads precede the reload
+      load(k + kRingSlots * nwarps, slot);
+    }
+  }
+}
+
 // ------------------------------------------------------ direct, bulk ---
 // The same run permutation moved by the Tensor Memory Accelerator: one thread
 // per CTA streams units (runs cut into <= kBulkChunk-byte pieces) through a
@@ -1166,7 +1270,10 @@ int launch_runs(symm_heap* h, size_t in_off, size_t out_off, uint32_t W, uint32_
                                                               h->spin_budget, ctl);
     return cuda_check(cudaGetLastError(), what);
   }
-  return symm_host::launch_runs_raw(in, out, h->slab, h->slab, W, Sb, R, inverse, s, what);
+  int rc = ensure_ctrl(h, s);  // the heap header records a wait that gives up
+  if (rc) return rc;
+  return symm_host::launch_runs_raw(in, out, h->slab, h->slab, W, Sb, R, inverse, s, what,
+                                    /*device_mem=*/true, h->base, h->spin_budget);
 }
 
 }  // namespace
@@ -1176,7 +1283,8 @@ int launch_runs(symm_heap* h, size_t in_off, size_t out_off, uint32_t W, uint32_
 // page-locked host memory reached over the host link).
 int symm_host::launch_runs_raw(const uint8_t* in, uint8_t* out, size_t in_pe, size_t out_pe,
                                uint32_t W, uint32_t Sb, size_t R, bool inverse, cudaStream_t s,
-                               const char* what) {
+                               const char* what, bool device_mem, void* ctl,
+                               uint64_t budget_ns) {
   const size_t nruns = (size_t)W * W * Sb;
   if (nruns == 0 || R == 0) return SYMM_OK;
   if (nruns > 0x7fffffffull) return fail(SYMM_EINVAL, std::string(what) + ": more than 2^31 runs");
@@ -1201,6 +1309,31 @@ int symm_host::launch_runs_raw(const uint8_t* in, uint8_t* out, size_t in_pe, si
       a2a_runs_batch_kernel<false><<<bgrid, kRunThreads, 0, s>>>(in, out, in_pe, out_pe, W, Sb,
                                                                  (uint32_t)R, (uint32_t)nruns, m);
     return cuda_check(cudaGetLastError(), what);
+  }
+  // unaligned runs of 1 KB up to a ring slot, in device memory: bulk loads
+  // of each run's covering range through a per-warp ring
+  const size_t ring_slot = (R + 30) & ~(size_t)15;
+  if (SYMM_RUNS_RING && !aligned && device_mem && ctl && R >= kRingMinRun &&
+      ring_slot <= kRingMaxSlot) {
+    const void* rfn = inverse ? (const void*)a2a_runs_ring_kernel<true>
+                              : (const void*)a2a_runs_ring_kernel<false>;
+    const size_t smem = kRingHeader + (size_t)kRingWarps * kRingSlots * ring_slot;
+    const int rcap = resident_ctas(rfn, 32 * kRingWarps, smem,
+                                   kRingHeader + (size_t)kRingWarps * kRingSlots * kRingMaxSlot);
+    if (rcap > 0) {
+      const size_t rneed = (nruns + kRingWarps - 1) / kRingWarps;
+      const int rgrid = (int)(rneed < (size_t)rcap ? rneed : (size_t)rcap);
+      Control* c = static_cast<Control*>(ctl);
+      if (inverse)
+        a2a_runs_ring_kernel<true><<<rgrid, 32 * kRingWarps, smem, s>>>(
+            in, out, in_pe, out_pe, W, Sb, (uint32_t)R, (uint32_t)nruns, (uint32_t)ring_slot,
+            budget_ns, c);
+      else
+        a2a_runs_ring_kernel<false><<<rgrid, 32 * kRingWarps, smem, s>>>(
+            in, out, in_pe, out_pe, W, Sb, (uint32_t)R, (uint32_t)nruns, (uint32_t)ring_slot,
+            budget_ns, c);
+      return cuda_check(cudaGetLastError(), what);
+    }
   }
   const void* kfn = inverse ? (aligned ? (const void*)a2a_runs_kernel<true, true>
                                        : (const void*)a2a_runs_kernel<true, false>)

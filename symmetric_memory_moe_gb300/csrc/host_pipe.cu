@@ -139,7 +139,8 @@ extern "C" int all2all_combine_host(symm_heap_t* h, const void* host_in, void* h
     void* dout = din ? mapped_host_range(hout, host_bytes) : nullptr;
     if (din && dout)  // the combine in place on the host buffers
       return launch_runs_raw(static_cast<const uint8_t*>(din), static_cast<uint8_t*>(dout),
-                             nbytes, nbytes, (uint32_t)W, (uint32_t)S, R, false, s, what);
+                             nbytes, nbytes, (uint32_t)W, (uint32_t)S, R, false, s, what,
+                             /*device_mem=*/false);
   }
 
   // chunks of cs rows, two buffers of W*cs rows inside each object

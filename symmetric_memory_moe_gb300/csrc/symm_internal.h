@@ -43,8 +43,13 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 
 // The direct run permutation (combine when !inverse, its inverse otherwise)
 // between two device-accessible buffers with PE strides in_pe and out_pe.
+// device_mem: both buffers are device memory, so bulk (TMA) copies may read
+// them (page-locked host memory is read with plain loads only); ctl (a heap
+// header, zeroed) and budget_ns: where a kernel with bounded waits records a
+// give-up -- without them only kernels that never wait are used.
 int launch_runs_raw(const uint8_t* in, uint8_t* out, size_t in_pe, size_t out_pe, uint32_t W,
-                    uint32_t Sb, size_t R, bool inverse, cudaStream_t s, const char* what);
+                    uint32_t Sb, size_t R, bool inverse, cudaStream_t s, const char* what,
+                    bool device_mem = true, void* ctl = nullptr, uint64_t budget_ns = 0);
 
 // One producer/consumer combine (all2all_combine's SYMM_A2A_PC and the
 // allocation-free entry point share it): PE k's input and output at
