@@ -204,16 +204,35 @@ __global__ void __launch_bounds__(kRunThreads, SYMM_RUNS_BATCH_MIN_BLOCKS)
 // bytes), completing on the slot's mbarrier; the warp then funnel-shifts the
 // slot into aligned 16-byte stores (byte heads and tails) and lane 0 reloads
 // the slot with the run kRingSlots ahead.  Device memory only.  Warps take
-// runs grid-stride in the order of a2a_runs_kernel.
+// runs grid-stride in the order of a2a_runs_kernel.  Shared memory bounds
+// the residency, so CTAs are small (4 warps of 2 slots: 28 warps on an SM
+// for the tail shape's 4 KB runs).
 #ifndef SYMM_RUNS_RING
 #define SYMM_RUNS_RING 1
 #endif
-constexpr int kRingWarps = 8;
-constexpr int kRingSlots = 3;
+#ifndef SYMM_RING_WARPS
+#define SYMM_RING_WARPS 4
+#endif
+#ifndef SYMM_RING_SLOTS
+#define SYMM_RING_SLOTS 2
+#endif
+#ifndef SYMM_RING_UNROLL
+#define SYMM_RING_UNROLL 2
+#endif
+#ifndef SYMM_RING_ORDER  // 0: consecutive warps write consecutive runs; 1: read them
+#define SYMM_RING_ORDER 0
+#endif
+constexpr int kRingWarps = SYMM_RING_WARPS;
+constexpr int kRingSlots = SYMM_RING_SLOTS;
+constexpr int kRingUnroll = SYMM_RING_UNROLL;
 constexpr uint32_t kRingMinRun = 1024;
-constexpr uint32_t kRingMaxSlot = 8192;
-constexpr uint32_t kRingHeader = 256;  // kRingWarps x kRingSlots mbarriers
-static_assert(kRingWarps * kRingSlots * 8 <= kRingHeader, "ring barriers fit the header");
+// kRingWarps x kRingSlots mbarriers, rounded up to 128 bytes
+constexpr uint32_t kRingHeader = (8u * kRingWarps * kRingSlots + 127u) & ~127u;
+// the largest slot: 8 KB, or what fits 227 KB of shared memory
+constexpr uint32_t kRingMaxSlot =
+    ((232448u - kRingHeader) / (kRingWarps * kRingSlots) & ~15u) < 8192u
+        ? ((232448u - kRingHeader) / (kRingWarps * kRingSlots) & ~15u)
+        : 8192u;
 template <bool INVERSE>
 __global__ void __launch_bounds__(32 * kRingWarps)
     a2a_runs_ring_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, size_t in_pe,
@@ -226,12 +245,23 @@ __global__ void __launch_bounds__(32 * kRingWarps)
   const uint32_t warp = blockIdx.x * kRingWarps + wib;
   const uint32_t nwarps = gridDim.x * kRingWarps;
   auto run_at = [&](uint32_t k, const uint8_t** src, uint8_t** dst) {
+    const bool r_fastest = (SYMM_RING_ORDER == 0) != INVERSE;
+    uint32_t r, s, d;
+    if (r_fastest) {
+      r = k % W;
+      const uint32_t t = k / W;
+      s = t % Sb;
+      d = t / Sb;
+    } else {
+      s = k % Sb;
+      const uint32_t t = k / Sb;
+      d = t % W;
+      r = t / W;
+    }
     if (!INVERSE) {
-      const uint32_t r = k % W, t = k / W, s = t % Sb, d = t / Sb;
       *src = in + r * in_pe + (size_t)(d * Sb + s) * R;
       *dst = out + d * out_pe + (size_t)(s * W + r) * R;
     } else {
-      const uint32_t s = k % Sb, t = k / Sb, d = t % W, r = t / W;
       *src = in + d * in_pe + (size_t)(s * W + r) * R;
       *dst = out + r * out_pe + (size_t)(d * Sb + s) * R;
     }
@@ -278,6 +308,7 @@ __global__ void __launch_bounds__(32 * kRingWarps)
     uint32_t head = (uint32_t)((16 - ((uintptr_t)dst & 15)) & 15);
     if (head > R) head = R;
     const uint32_t nvec = (R - head) >> 4, tail = R - head - (nvec << 4);
+#pragma unroll kRingUnroll
     for (uint32_t c = lane; c < nvec; c += 32) {
       const uint32_t q = m + head + 16 * c;
       const uint8_t* p = sl + (q & ~15u);
