@@ -195,18 +195,17 @@ __global__ void __launch_bounds__(kRunThreads, SYMM_RUNS_BATCH_MIN_BLOCKS)
 }
 
 // ----------------------------------------------- direct, unaligned runs ---
-// Runs that are not 16-byte aligned, of kRingMinRun bytes up to a slot: the
-// general instance above keeps only a few vectors in flight in registers
-// and is bound by memory latency.  Here each warp streams its runs through
-// its own ring of kRingSlots shared-memory slots: lane 0 loads the 16-byte-
-// aligned block range covering a run with one bulk (TMA) copy (at most 15
-// bytes on either side of the run, inside the granules of its first and last
-// bytes), completing on the slot's mbarrier; the warp then funnel-shifts the
-// slot into aligned 16-byte stores (byte heads and tails) and lane 0 reloads
-// the slot with the run kRingSlots ahead.  Device memory only.  Warps take
-// runs grid-stride in the order of a2a_runs_kernel.  Shared memory bounds
-// the residency, so CTAs are small (4 warps of 2 slots: 28 warps on an SM
-// for the tail shape's 4 KB runs).
+// Runs that are not 16-byte aligned, up to a slot: the general instance
+// above keeps only a few vectors in flight in registers and is bound by
+// memory latency.  Here each warp streams its runs (or batches of short
+// runs, below) through its own ring of kRingSlots shared-memory slots: lane
+// 0 loads the 16-byte-aligned block range covering a run with one bulk (TMA)
+// copy (at most 15 bytes on either side of the run, inside the granules of
+// its first and last bytes), completing on the slot's mbarrier; the warp
+// then funnel-shifts the slot into aligned 16-byte stores (byte heads and
+// tails) and lane 0 reloads the slot with the unit kRingSlots ahead.  Device
+// memory only.  Shared memory bounds the residency, so CTAs are small (4
+// warps of 2 slots: 28 warps on an SM for the tail shape's 4 KB runs).
 #ifndef SYMM_RUNS_RING
 #define SYMM_RUNS_RING 1
 #endif
@@ -225,7 +224,10 @@ __global__ void __launch_bounds__(kRunThreads, SYMM_RUNS_BATCH_MIN_BLOCKS)
 constexpr int kRingWarps = SYMM_RING_WARPS;
 constexpr int kRingSlots = SYMM_RING_SLOTS;
 constexpr int kRingUnroll = SYMM_RING_UNROLL;
-constexpr uint32_t kRingMinRun = 1024;
+#ifndef SYMM_RING_MIN_RUN
+#define SYMM_RING_MIN_RUN 1536
+#endif
+constexpr uint32_t kRingMinRun = SYMM_RING_MIN_RUN;
 // kRingWarps x kRingSlots mbarriers, rounded up to 128 bytes
 constexpr uint32_t kRingHeader = (8u * kRingWarps * kRingSlots + 127u) & ~127u;
 // the largest slot: 8 KB, or what fits 227 KB of shared memory
@@ -233,31 +235,38 @@ constexpr uint32_t kRingMaxSlot =
     ((232448u - kRingHeader) / (kRingWarps * kRingSlots) & ~15u) < 8192u
         ? ((232448u - kRingHeader) / (kRingWarps * kRingSlots) & ~15u)
         : 8192u;
-template <bool INVERSE>
+// Bytes of a batch of short runs, at most, by run length: large runs gain
+// from large bulk copies, short ones (more byte edges and index work per
+// byte in the copy-out) from the residency of smaller slots.
+#ifndef SYMM_RING_BATCH_BYTES
+#define SYMM_RING_BATCH_BYTES 8160
+#endif
+constexpr uint32_t kRingBatchBytes = SYMM_RING_BATCH_BYTES;  // runs of 384 bytes and up
+constexpr uint32_t kRingMidBatchBytes = 6144;                // 32 to 383 bytes
+constexpr uint32_t kRingTinyBatchBytes = 2048;               // under 32 bytes
+static_assert(kRingBatchBytes + 30 <= kRingMaxSlot, "a batch's covering range fits a slot");
+// BATCH: runs shorter than kRingMinRun travel in batches of up to `mb` runs
+// that are consecutive in the input (one input PE's rows: the combine's
+// source r, the inverse's destination d; a batch ends with that PE's runs),
+// one bulk copy per batch; groups of `glanes` lanes then write one run each.
+// Unit u is batch u % nbp of input PE u / nbp, so consecutive warps read
+// consecutive input.  Without BATCH a unit is one run, in a2a_runs_kernel's
+// order.
+template <bool INVERSE, bool BATCH>
 __global__ void __launch_bounds__(32 * kRingWarps)
     a2a_runs_ring_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, size_t in_pe,
-                         size_t out_pe, uint32_t W, uint32_t Sb, uint32_t R, uint32_t nruns,
-                         uint32_t slot_bytes, uint64_t budget_ns, Control* ctl) {
+                         size_t out_pe, uint32_t W, uint32_t Sb, uint32_t R, uint32_t nunits,
+                         uint32_t mb, uint32_t nbp, uint32_t glanes, uint32_t slot_bytes,
+                         uint64_t budget_ns, Control* ctl) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem) + wib * kRingSlots;
   uint8_t* ring = smem + kRingHeader + (size_t)wib * kRingSlots * slot_bytes;
   const uint32_t warp = blockIdx.x * kRingWarps + wib;
   const uint32_t nwarps = gridDim.x * kRingWarps;
-  auto run_at = [&](uint32_t k, const uint8_t** src, uint8_t** dst) {
-    const bool r_fastest = (SYMM_RING_ORDER == 0) != INVERSE;
-    uint32_t r, s, d;
-    if (r_fastest) {
-      r = k % W;
-      const uint32_t t = k / W;
-      s = t % Sb;
-      d = t / Sb;
-    } else {
-      s = k % Sb;
-      const uint32_t t = k / Sb;
-      d = t % W;
-      r = t / W;
-    }
+  const uint32_t period = W * Sb;  // runs of one input PE
+  // run (r, s, d) -> its source and destination
+  auto ends = [&](uint32_t r, uint32_t s, uint32_t d, const uint8_t** src, uint8_t** dst) {
     if (!INVERSE) {
       *src = in + r * in_pe + (size_t)(d * Sb + s) * R;
       *dst = out + d * out_pe + (size_t)(s * W + r) * R;
@@ -266,25 +275,82 @@ __global__ void __launch_bounds__(32 * kRingWarps)
       *dst = out + r * out_pe + (size_t)(d * Sb + s) * R;
     }
   };
-  auto load = [&](uint32_t k, int slot) {  // lane 0: run k's covering range into `slot`
+  // run t of input PE p (t counts that PE's runs in input order)
+  auto batch_run = [&](uint32_t p, uint32_t t, const uint8_t** src, uint8_t** dst) {
+    if (!INVERSE)
+      ends(p, t % Sb, t / Sb, src, dst);  // p = r, t = d*Sb + s
+    else
+      ends(t % W, t / W, p, src, dst);  // p = d, t = s*W + r
+  };
+  // unit u -> source of its first run and its run count
+  auto unit_at = [&](uint32_t u, const uint8_t** src, uint8_t** dst, uint32_t* cnt) {
+    if (BATCH) {
+      const uint32_t p = u / nbp, t0 = (u % nbp) * mb;
+      *cnt = min(mb, period - t0);
+      batch_run(p, t0, src, dst);
+    } else {
+      const bool r_fastest = (SYMM_RING_ORDER == 0) != INVERSE;
+      uint32_t r, s, d;
+      if (r_fastest) {
+        r = u % W;
+        const uint32_t t = u / W;
+        s = t % Sb;
+        d = t / Sb;
+      } else {
+        s = u % Sb;
+        const uint32_t t = u / Sb;
+        d = t % W;
+        r = t / W;
+      }
+      ends(r, s, d, src, dst);
+      *cnt = 1;
+    }
+  };
+  auto load = [&](uint32_t u, int slot) {  // lane 0: unit u's covering range into `slot`
     const uint8_t* src;
     uint8_t* dst;
-    run_at(k, &src, &dst);
+    uint32_t cnt;
+    unit_at(u, &src, &dst, &cnt);
     const uintptr_t lo = (uintptr_t)src & ~(uintptr_t)15;
-    const uint32_t n = (uint32_t)((((uintptr_t)src + R + 15) & ~(uintptr_t)15) - lo);
+    const uint32_t n =
+        (uint32_t)((((uintptr_t)src + (size_t)cnt * R + 15) & ~(uintptr_t)15) - lo);
     symm::mbar_arrive_expect_tx(&full[slot], n);
     symm::bulk_load(ring + (size_t)slot * slot_bytes, reinterpret_cast<const void*>(lo), n,
                     &full[slot]);
+  };
+  // one run: slot bytes [q0, q0 + R) to dst, by the G lanes gl = 0..G-1
+  auto copy_run = [&](const uint8_t* sl, uint32_t q0, uint8_t* dst, uint32_t gl, uint32_t G) {
+    uint32_t head = (uint32_t)((16 - ((uintptr_t)dst & 15)) & 15);
+    if (head > R) head = R;
+    const uint32_t nvec = (R - head) >> 4, tail = R - head - (nvec << 4);
+#pragma unroll kRingUnroll
+    for (uint32_t c = gl; c < nvec; c += G) {
+      const uint32_t q = q0 + head + 16 * c;
+      const uint8_t* p = sl + (q & ~15u);
+      uint4 x = *reinterpret_cast<const uint4*>(p);
+      if (q & 15) x = symm::funnel16(x, *reinterpret_cast<const uint4*>(p + 16), q & 15);
+      symm::st16_cs(dst + head + 16 * c, x);
+    }
+    if (!BATCH) {  // G = 32 > 15 >= head, tail
+      if (gl < head) symm::st1(dst + gl, sl[q0 + gl]);
+      if (gl < tail) symm::st1(dst + head + (nvec << 4) + gl, sl[q0 + head + (nvec << 4) + gl]);
+    } else {
+      for (uint32_t b = gl; b < head; b += G) symm::st1(dst + b, sl[q0 + b]);
+      for (uint32_t b = gl; b < tail; b += G) {
+        const uint32_t x = head + (nvec << 4) + b;
+        symm::st1(dst + x, sl[q0 + x]);
+      }
+    }
   };
   if (lane == 0) {
     for (int i = 0; i < kRingSlots; ++i) symm::mbar_init(&full[i], 1);
     symm::fence_mbar_init();
     for (int i = 0; i < kRingSlots; ++i)
-      if (warp + (uint64_t)i * nwarps < nruns) load(warp + i * nwarps, i);
+      if (warp + (uint64_t)i * nwarps < nunits) load(warp + i * nwarps, i);
   }
   __syncwarp();
   uint32_t it = 0;
-  for (uint32_t k = warp; k < nruns; k += nwarps, ++it) {
+  for (uint32_t u = warp; u < nunits; u += nwarps, ++it) {
     const int slot = (int)(it % kRingSlots);
     int ok = 1;
     if (lane == 0) ok = symm::mbar_wait(&full[slot], (it / kRingSlots) & 1u, budget_ns);
@@ -294,7 +360,7 @@ __global__ void __launch_bounds__(32 * kRingWarps)
       if (lane == 0) {
         symm::record_error(ctl, symm::kErrTimedOut, -1);
         // let this warp's loads still in flight land before it leaves (bounded)
-        for (uint32_t j = 0; j < (uint32_t)kRingSlots && k + (uint64_t)j * nwarps < nruns; ++j)
+        for (uint32_t j = 0; j < (uint32_t)kRingSlots && u + (uint64_t)j * nwarps < nunits; ++j)
           symm::mbar_wait(&full[(it + j) % kRingSlots], ((it + j) / kRingSlots) & 1u, budget_ns);
       }
       return;  // uniform across the warp
@@ -302,29 +368,26 @@ __global__ void __launch_bounds__(32 * kRingWarps)
     symm::mbar_try_wait(&full[slot], (it / kRingSlots) & 1u);  // every lane observes the phase
     const uint8_t* src;
     uint8_t* dst;
-    run_at(k, &src, &dst);
+    uint32_t cnt;
+    unit_at(u, &src, &dst, &cnt);
     const uint8_t* sl = ring + (size_t)slot * slot_bytes;
-    const uint32_t m = (uint32_t)((uintptr_t)src & 15);  // the run's first byte in the slot
-    uint32_t head = (uint32_t)((16 - ((uintptr_t)dst & 15)) & 15);
-    if (head > R) head = R;
-    const uint32_t nvec = (R - head) >> 4, tail = R - head - (nvec << 4);
-#pragma unroll kRingUnroll
-    for (uint32_t c = lane; c < nvec; c += 32) {
-      const uint32_t q = m + head + 16 * c;
-      const uint8_t* p = sl + (q & ~15u);
-      uint4 x = *reinterpret_cast<const uint4*>(p);
-      if (q & 15) x = symm::funnel16(x, *reinterpret_cast<const uint4*>(p + 16), q & 15);
-      symm::st16_cs(dst + head + 16 * c, x);
-    }
-    if ((uint32_t)lane < head) symm::st1(dst + lane, sl[m + lane]);
-    if ((uint32_t)lane < tail) {
-      const uint32_t x = head + (nvec << 4) + lane;
-      symm::st1(dst + x, sl[m + x]);
+    const uint32_t m0 = (uint32_t)((uintptr_t)src & 15);  // the unit's first byte in the slot
+    if (!BATCH) {
+      copy_run(sl, m0, dst, (uint32_t)lane, 32);
+    } else {
+      const uint32_t gl = (uint32_t)lane % glanes, groups = 32 / glanes;
+      const uint32_t p = u / nbp, t0 = (u % nbp) * mb;
+      for (uint32_t j = (uint32_t)lane / glanes; j < cnt; j += groups) {
+        const uint8_t* sj;
+        uint8_t* dj;
+        batch_run(p, t0 + j, &sj, &dj);
+        copy_run(sl, m0 + j * R, dj, gl, glanes);
+      }
     }
     __syncwarp();  // every lane has read the slot
-    if (lane == 0 && k + (uint64_t)kRingSlots * nwarps < nruns) {
+    if (lane == 0 && u + (uint64_t)kRingSlots * nwarps < nunits) {
       symm::fence_proxy_async_shared();  // those reads precede the reload
-      load(k + kRingSlots * nwarps, slot);
+      load(u + kRingSlots * nwarps, slot);
     }
   }
 }
@@ -1341,29 +1404,48 @@ int symm_host::launch_runs_raw(const uint8_t* in, uint8_t* out, size_t in_pe, si
                                                                  (uint32_t)R, (uint32_t)nruns, m);
     return cuda_check(cudaGetLastError(), what);
   }
-  // unaligned runs of 1 KB up to a ring slot, in device memory: bulk loads
-  // of each run's covering range through a per-warp ring
-  const size_t ring_slot = (R + 30) & ~(size_t)15;
-  if (SYMM_RUNS_RING && !aligned && device_mem && ctl && R >= kRingMinRun &&
-      ring_slot <= kRingMaxSlot) {
-    const void* rfn = inverse ? (const void*)a2a_runs_ring_kernel<true>
-                              : (const void*)a2a_runs_ring_kernel<false>;
-    const size_t smem = kRingHeader + (size_t)kRingWarps * kRingSlots * ring_slot;
-    const int rcap = resident_ctas(rfn, 32 * kRingWarps, smem,
-                                   kRingHeader + (size_t)kRingWarps * kRingSlots * kRingMaxSlot);
-    if (rcap > 0) {
-      const size_t rneed = (nruns + kRingWarps - 1) / kRingWarps;
-      const int rgrid = (int)(rneed < (size_t)rcap ? rneed : (size_t)rcap);
-      Control* c = static_cast<Control*>(ctl);
-      if (inverse)
-        a2a_runs_ring_kernel<true><<<rgrid, 32 * kRingWarps, smem, s>>>(
-            in, out, in_pe, out_pe, W, Sb, (uint32_t)R, (uint32_t)nruns, (uint32_t)ring_slot,
-            budget_ns, c);
-      else
-        a2a_runs_ring_kernel<false><<<rgrid, 32 * kRingWarps, smem, s>>>(
-            in, out, in_pe, out_pe, W, Sb, (uint32_t)R, (uint32_t)nruns, (uint32_t)ring_slot,
-            budget_ns, c);
-      return cuda_check(cudaGetLastError(), what);
+  // unaligned runs in device memory: bulk loads through per-warp rings, one
+  // run per slot from 1 KB up to a slot, batches of shorter runs below
+  if (SYMM_RUNS_RING && !aligned && device_mem && ctl) {
+    const bool batch = R < kRingMinRun;
+    const size_t period = (size_t)W * Sb;  // runs of one input PE
+    size_t mb = 1, units = nruns;
+    uint32_t glanes = 32;
+    if (batch) {
+      const size_t bytes = R < 32 ? kRingTinyBatchBytes
+                           : R < 384 ? kRingMidBatchBytes
+                                     : kRingBatchBytes;
+      mb = std::max((size_t)1, std::min(period, bytes / R));
+      const size_t nbp = (period + mb - 1) / mb;
+      units = (size_t)W * nbp;
+      while (glanes > 8 && R < 16u * glanes) glanes >>= 1;
+    }
+    const size_t slot = (mb * R + 30) & ~(size_t)15;
+    if (slot <= kRingMaxSlot) {
+      const void* rfn =
+          inverse ? (batch ? (const void*)a2a_runs_ring_kernel<true, true>
+                           : (const void*)a2a_runs_ring_kernel<true, false>)
+                  : (batch ? (const void*)a2a_runs_ring_kernel<false, true>
+                           : (const void*)a2a_runs_ring_kernel<false, false>);
+      const size_t smem = kRingHeader + (size_t)kRingWarps * kRingSlots * slot;
+      const int rcap = resident_ctas(rfn, 32 * kRingWarps, smem,
+                                     kRingHeader + (size_t)kRingWarps * kRingSlots * kRingMaxSlot);
+      if (rcap > 0) {
+        const size_t rneed = (units + kRingWarps - 1) / kRingWarps;
+        const int rgrid = (int)(rneed < (size_t)rcap ? rneed : (size_t)rcap);
+        const uint32_t nbp = (uint32_t)((period + mb - 1) / mb);
+        Control* c = static_cast<Control*>(ctl);
+        auto go = [&](auto kern) {
+          kern<<<rgrid, 32 * kRingWarps, smem, s>>>(in, out, in_pe, out_pe, W, Sb, (uint32_t)R,
+                                                   (uint32_t)units, (uint32_t)mb, nbp, glanes,
+                                                   (uint32_t)slot, budget_ns, c);
+        };
+        if (inverse)
+          batch ? go(a2a_runs_ring_kernel<true, true>) : go(a2a_runs_ring_kernel<true, false>);
+        else
+          batch ? go(a2a_runs_ring_kernel<false, true>) : go(a2a_runs_ring_kernel<false, false>);
+        return cuda_check(cudaGetLastError(), what);
+      }
     }
   }
   const void* kfn = inverse ? (aligned ? (const void*)a2a_runs_kernel<true, true>

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from symmetric_memory_moe_gb300 import abi, inputs
-from symmetric_memory_moe_gb300.torch_heap import CombineBuffers
+from symmetric_memory_moe_gb300.torch_heap import CombineBuffers, TorchSymmHeap
 
 pytestmark = pytest.mark.gpu
 
@@ -175,6 +175,57 @@ def test_short_run_batches(op, W, S, H, D):
         want = o.combine_back(xv.reshape(W, S, H * W, D), W, S, H, D)
     torch.cuda.synchronize()
     assert_bits_equal(heap.download(bufs.out, n), want.view(np.uint8).reshape(W, -1))
+    heap.close()
+
+
+@pytest.mark.parametrize("op,W,S,H,D,es,in_shift,out_shift", [
+    ("combine", 3, 5, 1, 3, 2, 0, 0),         # 6-byte runs: one batch holds a period
+    ("combine", 5, 7, 1, 17, 2, 0, 0),        # 34-byte runs, period of 35 in one batch
+    ("combine", 7, 40, 1, 130, 2, 0, 0),      # 260-byte runs: batches of 23, the last of 4
+    ("combine", 4, 64, 1, 250, 2, 0, 0),      # 500-byte runs: batches of 16, none ragged
+    ("combine", 3, 20, 1, 511, 2, 0, 0),      # 1022-byte runs: batches of 7, the last of 4
+    ("combine", 3, 9, 2, 256, 2, 3, 0),       # 1024-byte runs made unaligned: batches of 7
+    ("combine", 3, 9, 2, 384, 2, 3, 0),       # 1536-byte runs made unaligned: one run per slot
+    ("combine", 7, 40, 1, 130, 2, 5, 11),     # shifted bases on both sides
+    ("combine", 1, 50, 1, 13, 1, 1, 2),       # one PE: a period of S runs
+    ("combine", 16, 512, 1, 250, 2, 0, 0),    # 8192 batches: warps stride over several
+    ("dispatch", 6, 12, 3, 15, 2, 0, 0),      # 90-byte runs, S' = 2
+    ("dispatch", 4, 8, 1, 301, 2, 7, 3),      # 602-byte runs, shifted
+    ("combine_back", 4, 9, 1, 333, 2, 0, 0),  # inverse: 666-byte runs, batches of 12
+    ("combine_back", 5, 3, 1, 7, 1, 0, 9),    # inverse: 7-byte runs
+])
+def test_unaligned_run_rings(op, W, S, H, D, es, in_shift, out_shift):
+    """Runs that are not 16-byte aligned stream through per-warp shared-memory
+    rings: one run per slot from 1536 bytes, batches of runs consecutive in
+    the input below (2, 6 or 8 KB by run length; a batch ends with its input
+    PE's runs), written by groups of 8, 16 or 32 lanes.  S is the combine's S, dispatch's S or the inverse's
+    S'.  Bit-exact against the oracle, bytes around the output untouched."""
+    rows_in = {"combine": S * W, "dispatch": S, "combine_back": S * W}[op]
+    xe = _rand_bytes(W, rows_in, H, D, es, seed=W * 7 + S * 3 + D + in_shift)
+    n = rows_in * H * D * es
+    heap = TorchSymmHeap(W, abi.SYMM_HEAP_HEADER_BYTES + 2 * n + 4096)
+    pin, pout = heap.malloc(n + 64), heap.malloc(n + 64)  # room for the shifts
+    inp, out = pin + in_shift, pout + out_shift
+    heap.upload(inp, xe.reshape(W, -1))
+    heap.views(pout, n + 64).fill_(POISON)
+    xv = np.ascontiguousarray(xe.numpy()).view(np.dtype((np.void, es)))
+    o = oracle.load()
+    if op == "combine":
+        abi.all2all_combine(heap.handle, inp, out, W, S, H, D, es, abi.SYMM_A2A_DIRECT,
+                            16, 0, 2, 0, 0)
+        want = o.combine(xv.reshape(W, S * W, H, D), W, S, H, D)
+    elif op == "dispatch":
+        abi.all2all_dispatch(heap.handle, inp, out, W, S, H, D, es)
+        want = o.dispatch(xv.reshape(W, S, H, D), W, S, H, D)
+    else:
+        abi.all2all_combine_back(heap.handle, inp, out, W, S, H, D, es)
+        want = o.combine_back(xv.reshape(W, S, H * W, D), W, S, H, D)
+    torch.cuda.synchronize()
+    assert abi.symm_check_error(heap.handle)[0] == abi.SYMM_OK
+    got = heap.download(pout, n + 64)
+    assert_bits_equal(got[:, out_shift:out_shift + n].contiguous(),
+                      want.view(np.uint8).reshape(W, -1))
+    assert (got[:, :out_shift] == POISON).all() and (got[:, out_shift + n:] == POISON).all()
     heap.close()
 
 
