@@ -91,6 +91,12 @@ constexpr int kRunThreads = 256;
 constexpr int kPcThreads = 256;  // 4 producer warps + 4 consumer warps
 constexpr int kPcGroup = 128;
 constexpr int kPcMinBlocks = SYMM_PC_MIN_BLOCKS;
+// a2a_pc_kernel's residency for its kCopyRows and kCopyAligned instances
+// (kCopyAny keeps kPcMinBlocks: its shift-merge spills at 64 registers).
+// Four CTAs per SM give a CTA to each of the small shape's 512 tasks.
+#ifndef SYMM_PC_KERNEL_MIN_BLOCKS
+#define SYMM_PC_KERNEL_MIN_BLOCKS 4
+#endif
 
 // --------------------------------------------------------------- direct ---
 // One warp per run of R = H*D*elem_bytes contiguous bytes, destination-major.
@@ -697,7 +703,8 @@ constexpr uint32_t kPcAnyChunk = SYMM_PC_ANY_CHUNK;
 enum { kCopyRows = 0, kCopyAligned = 1, kCopyAny = 2 };
 
 template <bool PREFETCH, int MODE>
-__global__ void __launch_bounds__(kPcThreads, kPcMinBlocks)
+__global__ void __launch_bounds__(kPcThreads,
+                                  MODE == kCopyAny ? kPcMinBlocks : SYMM_PC_KERNEL_MIN_BLOCKS)
     a2a_pc_kernel(const PcArgs a, uint32_t tile_bytes) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int status[2];
