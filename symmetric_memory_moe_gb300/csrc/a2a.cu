@@ -251,14 +251,17 @@ constexpr uint32_t kRingBatchBytes = SYMM_RING_BATCH_BYTES;  // runs of 384 byte
 constexpr uint32_t kRingMidBatchBytes = 6144;                // 32 to 383 bytes
 constexpr uint32_t kRingTinyBatchBytes = 2048;               // under 32 bytes
 static_assert(kRingBatchBytes + 30 <= kRingMaxSlot, "a batch's covering range fits a slot");
-// BATCH: runs shorter than kRingMinRun travel in batches of up to `mb` runs
-// that are consecutive in the input (one input PE's rows: the combine's
-// source r, the inverse's destination d; a batch ends with that PE's runs),
-// one bulk copy per batch; groups of `glanes` lanes then write one run each.
-// Unit u is batch u % nbp of input PE u / nbp, so consecutive warps read
-// consecutive input.  Without BATCH a unit is one run, in a2a_runs_kernel's
-// order.
-template <bool INVERSE, bool BATCH>
+// MODE kRingPerRun: a unit is one run, in a2a_runs_kernel's order.  Runs
+// shorter than kRingMinRun travel in batches of up to `mb` runs that are
+// consecutive in the input (one input PE's rows: the combine's source r, the
+// inverse's destination d; a batch ends with that PE's runs), one bulk copy
+// per batch; unit u is batch u % nbp of input PE u / nbp, so consecutive
+// warps read consecutive input.  kRingBatchWarp: the whole warp writes the
+// batch's runs one after another (runs of 512 bytes and up);
+// kRingBatchGroups: groups of `glanes` lanes (8 or 16) write one run each.
+// (One instance per way of writing: sharing one, each slowed the other.)
+enum { kRingPerRun = 0, kRingBatchWarp = 1, kRingBatchGroups = 2 };
+template <bool INVERSE, int MODE>
 __global__ void __launch_bounds__(32 * kRingWarps)
     a2a_runs_ring_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out, size_t in_pe,
                          size_t out_pe, uint32_t W, uint32_t Sb, uint32_t R, uint32_t nunits,
@@ -281,19 +284,16 @@ __global__ void __launch_bounds__(32 * kRingWarps)
       *dst = out + r * out_pe + (size_t)(d * Sb + s) * R;
     }
   };
-  // run t of input PE p (t counts that PE's runs in input order)
-  auto batch_run = [&](uint32_t p, uint32_t t, const uint8_t** src, uint8_t** dst) {
-    if (!INVERSE)
-      ends(p, t % Sb, t / Sb, src, dst);  // p = r, t = d*Sb + s
-    else
-      ends(t % W, t / W, p, src, dst);  // p = d, t = s*W + r
-  };
   // unit u -> source of its first run and its run count
   auto unit_at = [&](uint32_t u, const uint8_t** src, uint8_t** dst, uint32_t* cnt) {
-    if (BATCH) {
+    if (MODE != kRingPerRun) {
+      // run t of input PE p (its runs in input order: the combine's
+      // t = d*Sb + s of source p, the inverse's t = s*W + r of destination p)
+      // starts at in + p*in_pe + t*R
       const uint32_t p = u / nbp, t0 = (u % nbp) * mb;
       *cnt = min(mb, period - t0);
-      batch_run(p, t0, src, dst);
+      *src = in + p * in_pe + (size_t)t0 * R;
+      *dst = nullptr;  // each run's own, in the copy-out
     } else {
       const bool r_fastest = (SYMM_RING_ORDER == 0) != INVERSE;
       uint32_t r, s, d;
@@ -325,7 +325,9 @@ __global__ void __launch_bounds__(32 * kRingWarps)
                     &full[slot]);
   };
   // one run: slot bytes [q0, q0 + R) to dst, by the G lanes gl = 0..G-1
-  auto copy_run = [&](const uint8_t* sl, uint32_t q0, uint8_t* dst, uint32_t gl, uint32_t G) {
+  // (whole: G = 32, more lanes than head or tail bytes)
+  auto copy_run = [&](const uint8_t* sl, uint32_t q0, uint8_t* dst, uint32_t gl, uint32_t G,
+                      bool whole) {
     uint32_t head = (uint32_t)((16 - ((uintptr_t)dst & 15)) & 15);
     if (head > R) head = R;
     const uint32_t nvec = (R - head) >> 4, tail = R - head - (nvec << 4);
@@ -337,7 +339,7 @@ __global__ void __launch_bounds__(32 * kRingWarps)
       if (q & 15) x = symm::funnel16(x, *reinterpret_cast<const uint4*>(p + 16), q & 15);
       symm::st16_cs(dst + head + 16 * c, x);
     }
-    if (!BATCH) {  // G = 32 > 15 >= head, tail
+    if (whole) {  // G = 32 > 15 >= head, tail
       if (gl < head) symm::st1(dst + gl, sl[q0 + gl]);
       if (gl < tail) symm::st1(dst + head + (nvec << 4) + gl, sl[q0 + head + (nvec << 4) + gl]);
     } else {
@@ -378,16 +380,38 @@ __global__ void __launch_bounds__(32 * kRingWarps)
     unit_at(u, &src, &dst, &cnt);
     const uint8_t* sl = ring + (size_t)slot * slot_bytes;
     const uint32_t m0 = (uint32_t)((uintptr_t)src & 15);  // the unit's first byte in the slot
-    if (!BATCH) {
-      copy_run(sl, m0, dst, (uint32_t)lane, 32);
+    if (MODE == kRingPerRun) {
+      copy_run(sl, m0, dst, (uint32_t)lane, 32, true);
     } else {
-      const uint32_t gl = (uint32_t)lane % glanes, groups = 32 / glanes;
       const uint32_t p = u / nbp, t0 = (u % nbp) * mb;
-      for (uint32_t j = (uint32_t)lane / glanes; j < cnt; j += groups) {
-        const uint8_t* sj;
-        uint8_t* dj;
-        batch_run(p, t0 + j, &sj, &dj);
-        copy_run(sl, m0 + j * R, dj, gl, glanes);
+      const uint32_t gl = (uint32_t)lane % glanes, groups = 32 / glanes;
+      uint32_t j = (uint32_t)lane / glanes;
+      if (MODE == kRingBatchWarp) {
+        for (; j < cnt; j += groups) {
+          const uint8_t* sj;
+          uint8_t* dj;
+          const uint32_t t = t0 + j;
+          if (!INVERSE)
+            ends(p, t % Sb, t / Sb, &sj, &dj);  // p = r, t = d*Sb + s
+          else
+            ends(t % W, t / W, p, &sj, &dj);  // p = d, t = s*W + r
+          copy_run(sl, m0 + j * R, dj, gl, glanes, false);
+        }
+      } else {
+        // run t = hi * L + lo: the combine's (d, s), the inverse's (s, r); a
+        // cursor per lane group steps `groups` runs without dividing
+        const uint32_t L = INVERSE ? W : Sb;
+        uint32_t hi = (t0 + j) / L, lo = (t0 + j) - hi * L;
+        for (; j < cnt; j += groups) {
+          uint8_t* dj = INVERSE ? out + lo * out_pe + (size_t)(p * Sb + hi) * R
+                                : out + hi * out_pe + (size_t)(lo * W + p) * R;
+          copy_run(sl, m0 + j * R, dj, gl, glanes, false);
+          lo += groups;
+          while (lo >= L) {
+            lo -= L;
+            ++hi;
+          }
+        }
       }
     }
     __syncwarp();  // every lane has read the slot
@@ -1429,11 +1453,15 @@ int symm_host::launch_runs_raw(const uint8_t* in, uint8_t* out, size_t in_pe, si
     }
     const size_t slot = (mb * R + 30) & ~(size_t)15;
     if (slot <= kRingMaxSlot) {
-      const void* rfn =
-          inverse ? (batch ? (const void*)a2a_runs_ring_kernel<true, true>
-                           : (const void*)a2a_runs_ring_kernel<true, false>)
-                  : (batch ? (const void*)a2a_runs_ring_kernel<false, true>
-                           : (const void*)a2a_runs_ring_kernel<false, false>);
+      const int mode = !batch ? kRingPerRun : glanes == 32 ? kRingBatchWarp : kRingBatchGroups;
+      const void* const fns[2][3] = {
+          {(const void*)a2a_runs_ring_kernel<false, kRingPerRun>,
+           (const void*)a2a_runs_ring_kernel<false, kRingBatchWarp>,
+           (const void*)a2a_runs_ring_kernel<false, kRingBatchGroups>},
+          {(const void*)a2a_runs_ring_kernel<true, kRingPerRun>,
+           (const void*)a2a_runs_ring_kernel<true, kRingBatchWarp>,
+           (const void*)a2a_runs_ring_kernel<true, kRingBatchGroups>}};
+      const void* rfn = fns[inverse ? 1 : 0][mode];
       const size_t smem = kRingHeader + (size_t)kRingWarps * kRingSlots * slot;
       const int rcap = resident_ctas(rfn, 32 * kRingWarps, smem,
                                      kRingHeader + (size_t)kRingWarps * kRingSlots * kRingMaxSlot);
@@ -1448,9 +1476,13 @@ int symm_host::launch_runs_raw(const uint8_t* in, uint8_t* out, size_t in_pe, si
                                                    (uint32_t)slot, budget_ns, c);
         };
         if (inverse)
-          batch ? go(a2a_runs_ring_kernel<true, true>) : go(a2a_runs_ring_kernel<true, false>);
+          mode == kRingPerRun      ? go(a2a_runs_ring_kernel<true, kRingPerRun>)
+          : mode == kRingBatchWarp ? go(a2a_runs_ring_kernel<true, kRingBatchWarp>)
+                                   : go(a2a_runs_ring_kernel<true, kRingBatchGroups>);
         else
-          batch ? go(a2a_runs_ring_kernel<false, true>) : go(a2a_runs_ring_kernel<false, false>);
+          mode == kRingPerRun      ? go(a2a_runs_ring_kernel<false, kRingPerRun>)
+          : mode == kRingBatchWarp ? go(a2a_runs_ring_kernel<false, kRingBatchWarp>)
+                                   : go(a2a_runs_ring_kernel<false, kRingBatchGroups>);
         return cuda_check(cudaGetLastError(), what);
       }
     }
