@@ -193,6 +193,10 @@ def test_short_run_batches(op, W, S, H, D):
     ("dispatch", 4, 8, 1, 301, 2, 7, 3),      # 602-byte runs, shifted
     ("combine_back", 4, 9, 1, 333, 2, 0, 0),  # inverse: 666-byte runs, batches of 12
     ("combine_back", 5, 3, 1, 7, 1, 0, 9),    # inverse: 7-byte runs
+    ("combine", 1, 1, 1, 5, 2, 3, 0),         # a single 10-byte run
+    ("combine_back", 1, 4, 1, 300, 2, 0, 5),  # inverse on one PE: 600-byte runs
+    ("dispatch", 3, 3, 1, 700, 2, 1, 0),      # 1400-byte runs, S' = 1: whole-warp batches of 3
+    ("combine_back", 4, 9, 1, 100, 2, 6, 2),  # inverse, 200-byte runs: groups of 8 lanes, shifted
 ])
 def test_unaligned_run_rings(op, W, S, H, D, es, in_shift, out_shift):
     """Runs that are not 16-byte aligned stream through per-warp shared-memory
