@@ -205,9 +205,9 @@ __global__ void __launch_bounds__(kRunThreads, SYMM_RUNS_BATCH_MIN_BLOCKS)
 // above keeps only a few vectors in flight in registers and is bound by
 // memory latency.  Here each warp streams its runs (or batches of short
 // runs, below) through its own ring of kRingSlots shared-memory slots: lane
-// 0 loads the 16-byte-aligned block range covering a run with one bulk (TMA)
-// copy (at most 15 bytes on either side of the run, inside the granules of
-// its first and last bytes), completing on the slot's mbarrier; the warp
+// 0 loads the 16-byte-aligned block range covering a unit with one bulk (TMA)
+// copy (at most 15 bytes on either side, inside the granules of the unit's
+// first and last bytes), completing on the slot's mbarrier; the warp
 // then funnel-shifts the slot into aligned 16-byte stores (byte heads and
 // tails) and lane 0 reloads the slot with the unit kRingSlots ahead.  Device
 // memory only.  Shared memory bounds the residency, so CTAs are small (4
