@@ -237,3 +237,24 @@ def test_header_is_plain_c(tmp_path):
                           "-fsyntax-only", "-I", os.path.join(ROOT, "include"), str(src)],
                          capture_output=True, text=True)
     assert res.returncode == 0, res.stderr
+
+
+def test_readme_example_uses_the_binding():
+    """The README's usage example parses, and every `abi.` name and heap
+    method it calls exists in the binding."""
+    import ast
+
+    from symmetric_memory_moe_gb300 import torch_heap
+
+    text = open(os.path.join(ROOT, "README.md")).read()
+    blocks = re.findall(r"```python\n(.*?)```", text, re.S)
+    assert blocks, "README has no python example"
+    for code in blocks:
+        tree = ast.parse(code)
+        for node in ast.walk(tree):
+            if isinstance(node, ast.Attribute) and isinstance(node.value, ast.Name):
+                if node.value.id == "abi":
+                    assert hasattr(abi, node.attr), f"abi.{node.attr}"
+                if node.value.id == "heap":
+                    assert hasattr(torch_heap.TorchSymmHeap, node.attr) or node.attr == "handle", \
+                        f"heap.{node.attr}"
