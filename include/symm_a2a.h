@@ -59,12 +59,16 @@ extern "C" {
  * (the caller has zeroed the signal slots itself) */
 #define SYMM_A2A_FLAG_NO_RESET 0x100
 /* Copy paths.  By default each variant uses the path measured fastest on
- * GB300: DIRECT moves 16-byte vectors through registers; PC prefetches the
- * producer's input tiles with bulk (TMA) copies into shared memory when
- * every tile row is 16-byte aligned (16-byte vectors otherwise).
+ * GB300: DIRECT moves 16-byte vectors through registers where every run is
+ * 16-byte aligned, and otherwise (in device memory) bulk-loads each run's, or
+ * each batch of short runs', 16-byte-aligned covering range into shared
+ * memory and stores aligned 16-byte vectors from there; PC prefetches the
+ * producer's input tiles with bulk (TMA) copies into shared memory when its
+ * rows are long enough to pay (2 KB aligned, 1 KB at any alignment), and
+ * uses 16-byte vectors otherwise.
  * OR-ed into the variant: SYMM_A2A_FLAG_VECTOR makes PC use 16-byte vectors
  * only; SYMM_A2A_FLAG_BULK makes DIRECT use bulk (TMA) copies through
- * shared memory where every run is 16-byte aligned. */
+ * shared memory both ways where every run is 16-byte aligned. */
 #define SYMM_A2A_FLAG_VECTOR 0x200
 #define SYMM_A2A_FLAG_BULK 0x400
 /* OR-ed into SYMM_A2A_PC, for debugging: a barrier between producers and
