@@ -255,10 +255,9 @@ static_assert(kRingBatchBytes + 30 <= kRingMaxSlot, "a batch's covering range fi
 // shorter than kRingMinRun travel in batches of up to `mb` runs that are
 // consecutive in the input (one input PE's rows: the combine's source r, the
 // inverse's destination d; a batch ends with that PE's runs), one bulk copy
-// per batch; unit u is batch u % nbp of input PE u / nbp, so consecutive
-// warps read consecutive input.  kRingBatchWarp: the whole warp writes the
-// batch's runs one after another (runs of 512 bytes and up);
-// kRingBatchGroups: groups of `glanes` lanes (8 or 16) write one run each.
+// per batch.  kRingBatchWarp: the whole warp writes the batch's runs one
+// after another (runs of 512 bytes and up); kRingBatchGroups: groups of
+// `glanes` lanes (8 or 16) write one run each.
 // (One instance per way of writing: sharing one, each slowed the other.)
 enum { kRingPerRun = 0, kRingBatchWarp = 1, kRingBatchGroups = 2 };
 template <bool INVERSE, int MODE>
@@ -290,7 +289,12 @@ __global__ void __launch_bounds__(32 * kRingWarps)
       // run t of input PE p (its runs in input order: the combine's
       // t = d*Sb + s of source p, the inverse's t = s*W + r of destination p)
       // starts at in + p*in_pe + t*R
-      const uint32_t p = u / nbp, t0 = (u % nbp) * mb;
+      // whole-warp batches: unit u is batch u / W of PE u % W, so output runs
+      // that share a boundary sector (same d and s, next r) are written by
+      // warps at work at the same time; lane-group batches: batch u % nbp of
+      // PE u / nbp, consecutive warps reading consecutive input
+      const uint32_t p = MODE == kRingBatchWarp ? u % W : u / nbp;
+      const uint32_t t0 = (MODE == kRingBatchWarp ? u / W : u % nbp) * mb;
       *cnt = min(mb, period - t0);
       *src = in + p * in_pe + (size_t)t0 * R;
       *dst = nullptr;  // each run's own, in the copy-out
@@ -383,7 +387,8 @@ __global__ void __launch_bounds__(32 * kRingWarps)
     if (MODE == kRingPerRun) {
       copy_run(sl, m0, dst, (uint32_t)lane, 32, true);
     } else {
-      const uint32_t p = u / nbp, t0 = (u % nbp) * mb;
+      const uint32_t p = MODE == kRingBatchWarp ? u % W : u / nbp;
+      const uint32_t t0 = (MODE == kRingBatchWarp ? u / W : u % nbp) * mb;
       const uint32_t gl = (uint32_t)lane % glanes, groups = 32 / glanes;
       uint32_t j = (uint32_t)lane / glanes;
       if (MODE == kRingBatchWarp) {
